@@ -1,0 +1,175 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV cache decode path for GB300 (sm_103a).
+ *
+ * Two operations, both asynchronous on the caller's CUDA stream:
+ *
+ *  paged_kv_append         writes each sequence's newest token K/V into its
+ *                          slot of the block pool;
+ *  paged_decode_attention  attends every sequence's newest query over all of
+ *                          its cached tokens, gathered through its block table.
+ *
+ * Sources (page title, section):
+ *  - "Distributed LLM Inference Serving Platform", section 2 (Mental Model &
+ *    Architectural Abstraction): a sequence's KV cache is split into
+ *    fixed-size logical blocks (16 tokens) mapped to non-contiguous physical
+ *    blocks of one HBM pool by a per-sequence block table; prompt blocks may
+ *    be shared by several sequences (copy-on-write, reference counts).
+ *  - same page, section 3 (Core Terminology, PagedAttention row): the
+ *    attention kernel reads K and V through the page tables.
+ *  - same page, section 5.1 (End-to-End Request Lifecycle): each decode step
+ *    every active sequence submits its latest token, its K/V are written into
+ *    the assigned physical block (a new block when the tail block is full),
+ *    and attention runs over all blocks in the sequence's table.
+ *  - same page, section 1 and the Lab 3 roofline solution (nHeads = 64,
+ *    nKvHeads = 8): grouped-query attention, query head h reads KV head
+ *    h / (n_q_heads / n_kv_heads).
+ *  - "Roadmap: vLLM-style serving features for TornadoVM batched decode",
+ *    Serving / scheduling list: block-pool KV with a per-slot block table.
+ *
+ * Data layout (the pages fix none; this is the library's reading):
+ *  - k_cache, v_cache: fp16 (IEEE binary16) [num_blocks][n_kv_heads]
+ *    [block_size][head_dim], contiguous.  Token t of sequence b, KV head j
+ *    lives at row t % block_size of physical block block_tables[b][t /
+ *    block_size].
+ *  - block_tables: int32 [num_seqs][max_blocks_per_seq], row-major.  Only the
+ *    first ceil(context_lens[b] / block_size) entries of row b are read.
+ *  - context_lens: int32 [num_seqs]; sequence b attends tokens
+ *    [0, context_lens[b]) -- the token appended this step included.
+ *  - slot_mapping: int64 [num_tokens]; slot = physical_block * block_size +
+ *    row; a negative slot marks a padding token that is skipped.
+ *  - q, out: fp16 [num_seqs][n_q_heads][head_dim]; k_new, v_new: fp16
+ *    [num_tokens][n_kv_heads][head_dim]; lse_out: fp32 [num_seqs][n_q_heads].
+ *
+ * Ownership: every pointer is a device pointer the caller allocates and owns
+ * (except where a host pointer is stated).  The library allocates no memory
+ * and keeps no state besides a cached per-device attribute lookup.  Tensor
+ * pointers (q, out, caches, k_new, v_new) must be 16-byte aligned.
+ *
+ * Errors: a call that detects a bad argument on the host returns a negative
+ * pkv_status and launches nothing.  Problems only the device can see (a
+ * block id outside [0, num_blocks), a slot beyond the pool, a context length
+ * outside [0, max_blocks_per_seq * block_size] or above max_context_len, a
+ * copy that did not complete within about a second) set bits in the optional
+ * device word *err_word (PKV_ERRBIT_*): the offending block or token is
+ * skipped, nothing traps, and the result for that sequence is unspecified.
+ * Read the word with paged_kv_get_error.  Launch failures return
+ * PKV_ERR_CUDA.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1, /* null or misaligned pointer, bad size, n_q % n_kv != 0 */
+    PKV_ERR_UNSUPPORTED = -2, /* head_dim, block_size or group size not built */
+    PKV_ERR_WORKSPACE = -3,   /* workspace missing or smaller than paged_decode_plan says */
+    PKV_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+    PKV_ERR_INDEX = -5        /* the device flagged a bad index (see the error word) */
+} pkv_status;
+
+/* Bits of the device error word. */
+#define PKV_ERRBIT_BLOCK_ID 0x1 /* block table entry outside [0, num_blocks) */
+#define PKV_ERRBIT_SLOT 0x2     /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_ERRBIT_CONTEXT 0x4  /* context length < 0, > max_blocks_per_seq*block_size,
+                                   or > max_context_len */
+#define PKV_ERRBIT_TIMEOUT 0x8  /* a bounded wait for a block copy gave up */
+
+/*
+ * Slot-mapped append ("Distributed LLM Inference Serving Platform", section
+ * 5.1, Chunked Prefill and Continuous Decode Loop items): for token i and KV
+ * head j, copies k_new[i][j][:] and v_new[i][j][:] bit for bit into row
+ * slot_mapping[i] % block_size of physical block slot_mapping[i] / block_size.
+ *
+ *  k_new, v_new   device, fp16 [num_tokens][n_kv_heads][head_dim]
+ *  slot_mapping   device, int64 [num_tokens]; < 0 = skip
+ *  k_cache, v_cache device, fp16 [num_blocks][n_kv_heads][block_size][head_dim]
+ *  head_dim       a multiple of 8
+ *  err_word       device int32, may be NULL; PKV_ERRBIT_SLOT is or-ed in for a
+ *                 slot >= num_blocks * block_size (that token is skipped)
+ *  cuda_stream    cudaStream_t (NULL = legacy default stream)
+ * Two tokens with the same slot in one call: which one lands is unspecified.
+ * num_tokens == 0 is a no-op.
+ */
+int paged_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                    void *k_cache, void *v_cache, int num_tokens, int n_kv_heads,
+                    int head_dim, int block_size, int64_t num_blocks, int32_t *err_word,
+                    void *cuda_stream);
+
+/*
+ * Split planning for paged_decode_attention (host only; no device work).
+ * partition_tokens = 0 asks for the automatic choice, which depends on the
+ * current device's SM count (a CUDA query; fails with PKV_ERR_CUDA when no
+ * device is present).  A nonzero partition_tokens is checked and echoed:
+ * it must be a positive multiple of 16 and of block_size with
+ * partition_tokens / block_size <= 2048.
+ *  max_context_len <= 0 means max_blocks_per_seq * block_size.
+ *  *partition_tokens_out  (host, may be NULL) tokens per split-K partition
+ *  *workspace_bytes_out   (host, may be NULL) workspace the call needs; 0 when
+ *                         every sequence fits one partition
+ */
+int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                      int block_size, int max_blocks_per_seq, int max_context_len,
+                      int partition_tokens, int *partition_tokens_out,
+                      size_t *workspace_bytes_out);
+
+/*
+ * Paged decode attention ("Distributed LLM Inference Serving Platform",
+ * sections 2, 3 and 5.1; grouped-query mapping from section 1):
+ *
+ *   out[b][h][:] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,  t in [0, L_b)
+ *
+ * with K_t, V_t the rows of KV head h / (n_q_heads / n_kv_heads) gathered
+ * through block_tables[b].  Logits and the softmax run in fp32 (online
+ * max/sum rescaling); the output is rounded to fp16 (round to nearest even).
+ * Long contexts are split into partitions of partition_tokens tokens whose
+ * partial results are merged by log-sum-exp (flash-decoding split).
+ * L_b = 0 gives out = 0 and lse = -inf.
+ *
+ *  out            device fp16 [num_seqs][n_q_heads][head_dim]
+ *  q              device fp16 [num_seqs][n_q_heads][head_dim]
+ *  k_cache, v_cache, block_tables, context_lens   as in the layout notes
+ *  scale          multiplies q . K before the softmax (1/sqrt(head_dim) usually)
+ *  head_dim       64 or 128;  block_size 1, 2, 4, 8, 16, 32, 64, 128 or 256;
+ *                 n_q_heads / n_kv_heads in {1, 2, 4, 8}
+ *  max_context_len an upper bound on every context length (no device sync
+ *                 is needed to know it); <= 0 means max_blocks_per_seq*block_size
+ *  partition_tokens 0 = automatic (see paged_decode_plan)
+ *  workspace      device scratch of at least the planned bytes (16-byte
+ *                 aligned), may be NULL when the plan needs 0 bytes; the
+ *                 caller owns it; calls that overlap in time need separate
+ *                 workspaces
+ *  lse_out        device fp32 [num_seqs][n_q_heads] natural-log sum of
+ *                 exp(logits), may be NULL
+ *  err_word       device int32, may be NULL (see the header comment)
+ *  cuda_stream    cudaStream_t
+ */
+int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           int num_seqs, int max_blocks_per_seq, int64_t num_blocks,
+                           float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                           int block_size, int max_context_len, int partition_tokens,
+                           void *workspace, size_t workspace_bytes, float *lse_out,
+                           int32_t *err_word, void *cuda_stream);
+
+/*
+ * Reads the device error word: waits for cuda_stream, copies *err_word to the
+ * host, stores it in *bits_out (host, may be NULL) and returns PKV_OK when it
+ * is 0, PKV_ERR_INDEX otherwise.  Does not clear the word.
+ */
+int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits_out);
+
+/* Static English text for a pkv_status value. */
+const char *paged_kv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

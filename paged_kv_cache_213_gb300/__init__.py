@@ -1,1 +1,23 @@
-"""paged_kv_cache_213_gb300 -- paged decode attention for GB300 (sm_103a)."""
+"""paged_kv_cache_213_gb300 -- paged decode attention for GB300 (sm_103a).
+
+The compute lives in hand-written CUDA kernels behind a C ABI
+(``include/pagedkv.h``, built into ``_build/libpagedkv.so``).  The Python
+functions here only marshal torch tensors to that ABI; there is no CPU
+fallback.  The library is loaded on first use, which raises if it was not
+built.
+"""
+from .binding import (  # noqa: F401
+    PKV_ERRBIT_BLOCK_ID,
+    PKV_ERRBIT_CONTEXT,
+    PKV_ERRBIT_SLOT,
+    PKV_ERRBIT_TIMEOUT,
+    PagedKVError,
+    decode_plan,
+    default_scale,
+    get_error,
+    library,
+    library_path,
+    paged_decode_attention,
+    paged_kv_append,
+    status_string,
+)

@@ -1,0 +1,219 @@
+"""ctypes binding of ``libpagedkv.so`` (the C ABI in ``include/pagedkv.h``).
+
+Argument marshalling only: shapes, dtypes, device and contiguity checks,
+data pointers, the current torch stream, and torch allocation of outputs and
+workspace.  Every step of the computation runs in the library's CUDA
+kernels.  There is no CPU fallback: if the library is missing, or a tensor
+is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libpagedkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_WORKSPACE = -3
+PKV_ERR_CUDA = -4
+PKV_ERR_INDEX = -5
+
+PKV_ERRBIT_BLOCK_ID = 0x1
+PKV_ERRBIT_SLOT = 0x2
+PKV_ERRBIT_CONTEXT = 0x4
+PKV_ERRBIT_TIMEOUT = 0x8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    """A library call returned a negative status."""
+
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it first "
+                "(python -m paged_kv_cache_213_gb300.build, or __graft_entry__.build())")
+        lib = ctypes.CDLL(_LIB_PATH)
+        c = ctypes
+        p = c.c_void_p
+        lib.paged_kv_append.argtypes = [p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int,
+                                        c.c_int64, p, p]
+        lib.paged_kv_append.restype = c.c_int
+        lib.paged_decode_plan.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                                          c.c_int, c.c_int, c.POINTER(c.c_int),
+                                          c.POINTER(c.c_size_t)]
+        lib.paged_decode_plan.restype = c.c_int
+        lib.paged_decode_attention.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64,
+                                               c.c_float, c.c_int, c.c_int, c.c_int, c.c_int,
+                                               c.c_int, c.c_int, p, c.c_size_t, p, p, p]
+        lib.paged_decode_attention.restype = c.c_int
+        lib.paged_kv_get_error.argtypes = [p, p, c.POINTER(c.c_int32)]
+        lib.paged_kv_get_error.restype = c.c_int
+        lib.paged_kv_status_string.argtypes = [c.c_int]
+        lib.paged_kv_status_string.restype = c.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return library().paged_kv_status_string(int(status)).decode()
+
+
+def _check(func: str, status: int):
+    if status != PKV_OK:
+        raise PagedKVError(func, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def paged_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, err_word=None):
+    """Write k_new/v_new [T, Hk, d] (fp16) into slots slot_mapping [T] (int64)
+    of k_cache/v_cache [NB, Hk, bs, d] (fp16), in place, on the current stream."""
+    dev = k_cache.device
+    _need(k_new, "k_new", torch.float16, dev)
+    _need(v_new, "v_new", torch.float16, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    _need(k_cache, "k_cache", torch.float16, dev)
+    _need(v_cache, "v_cache", torch.float16, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must both be [num_blocks, n_kv_heads, block_size, head_dim]")
+    NB, Hk, bs, d = k_cache.shape
+    if k_new.dim() != 3 or k_new.shape[1:] != (Hk, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens, n_kv_heads, head_dim]")
+    T = k_new.shape[0]
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    with torch.cuda.device(dev):
+        rc = library().paged_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                       _ptr(k_cache), _ptr(v_cache), T, Hk, d, bs, NB,
+                                       _ptr(err_word), _stream_handle(dev))
+    _check("paged_kv_append", rc)
+
+
+def decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                max_context_len=0, partition_tokens=0):
+    """(partition_tokens, workspace_bytes) the library will use."""
+    P = ctypes.c_int(0)
+    W = ctypes.c_size_t(0)
+    rc = library().paged_decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                     max_blocks_per_seq, max_context_len, partition_tokens,
+                                     ctypes.byref(P), ctypes.byref(W))
+    _check("paged_decode_plan", rc)
+    return P.value, W.value
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, n_q_heads,
+                           n_kv_heads, head_dim, block_size, max_context_len=None,
+                           partition_tokens=0, out=None, workspace=None, lse=None,
+                           err_word=None):
+    """softmax(q K^T * scale) V over each sequence's paged K/V -> out [B, H, d] fp16.
+
+    q [B, H, d] fp16; k_cache/v_cache [NB, Hk, bs, d] fp16; block_tables
+    [B, MB] int32; context_lens [B] int32.  max_context_len: an upper bound on
+    context_lens (None -> MB * bs; pass the host-side value to keep the launch
+    free of a device sync).  lse: optional fp32 [B, H] output tensor.
+    """
+    dev = q.device
+    _need(q, "q", torch.float16, dev)
+    _need(k_cache, "k_cache", torch.float16, dev)
+    _need(v_cache, "v_cache", torch.float16, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    B = q.shape[0]
+    if q.dim() != 3 or q.shape[1:] != (n_q_heads, head_dim):
+        raise ValueError("q must be [num_seqs, n_q_heads, head_dim]")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or \
+            k_cache.shape[1:] != (n_kv_heads, block_size, head_dim):
+        raise ValueError("caches must be [num_blocks, n_kv_heads, block_size, head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, MB], context_lens [B]")
+    MB = block_tables.shape[1]
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    P, ws_bytes = decode_plan(B, n_q_heads, n_kv_heads, head_dim, block_size, MB, mcl,
+                              partition_tokens)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+        if lse.shape != (B, n_q_heads):
+            raise ValueError("lse must be [B, H]")
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    if ws_bytes > 0:
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        else:
+            _need(workspace, "workspace", torch.uint8, dev)
+    with torch.cuda.device(dev):
+        rc = library().paged_decode_attention(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), n_q_heads, n_kv_heads,
+            head_dim, block_size, mcl, P, _ptr(workspace) if ws_bytes > 0 else None,
+            workspace.numel() if (ws_bytes > 0) else 0, _ptr(lse), _ptr(err_word),
+            _stream_handle(dev))
+    _check("paged_decode_attention", rc)
+    return out
+
+
+def get_error(err_word: torch.Tensor) -> int:
+    """Wait for the current stream and return the device error word's bits."""
+    _need(err_word, "err_word", torch.int32)
+    bits = ctypes.c_int32(0)
+    with torch.cuda.device(err_word.device):
+        rc = library().paged_kv_get_error(_ptr(err_word), _stream_handle(err_word.device),
+                                          ctypes.byref(bits))
+    if rc not in (PKV_OK, PKV_ERR_INDEX):
+        _check("paged_kv_get_error", rc)
+    return int(bits.value)
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,211 @@
+// api.cu -- the extern "C" entry points declared in include/pagedkv.h:
+// argument checks on the host, split planning, kernel launches on the
+// caller's stream.  Allocates nothing.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool block_size_ok(int bs) {
+    return bs == 1 || bs == 2 || bs == 4 || bs == 8 || bs == 16 || bs == 32 || bs == 64 ||
+           bs == 128 || bs == 256;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count(int *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *out = cached;
+            return PKV_OK;
+        }
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return PKV_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    *out = n;
+    return PKV_OK;
+}
+
+// Tokens per partition when the caller leaves the choice to the library:
+// the largest power of two in [128, 2048] (and >= the block size) that still
+// gives an upper-bound grid of at least 12 CTAs per SM, and no larger than
+// the longest context needs.
+int auto_partition(int num_seqs, int n_kv_heads, int max_len, int block_size, int sms) {
+    const int step = block_size > 16 ? block_size : 16;
+    int P = 2048;
+    while (P > 128 && P / 2 >= step) {
+        const long long parts = (max_len + P - 1) / P;
+        if (static_cast<long long>(num_seqs) * n_kv_heads * parts >= 12LL * sms) break;
+        P /= 2;
+    }
+    const int cover = (max_len + step - 1) / step * step;  // one partition suffices
+    if (cover > 0 && cover < P) P = cover;
+    return P < step ? step : P;
+}
+
+struct Plan {
+    int max_len;
+    int partition;
+    int max_parts;
+    size_t ws_bytes;
+};
+
+int make_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+              int max_blocks_per_seq, int max_context_len, int partition_tokens, Plan *plan) {
+    if (num_seqs < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
+        max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (!block_size_ok(block_size)) return PKV_ERR_UNSUPPORTED;
+    if (!pkv::decode_supported(head_dim, n_q_heads / n_kv_heads)) return PKV_ERR_UNSUPPORTED;
+    const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+    if (cap > (1LL << 30)) return PKV_ERR_INVALID_ARG;
+    long long max_len = max_context_len <= 0 ? cap : max_context_len;
+    if (max_len > cap) max_len = cap;
+    int P = partition_tokens;
+    if (P == 0) {
+        int sms = 0;
+        const int rc = sm_count(&sms);
+        if (rc != PKV_OK) return rc;
+        P = auto_partition(num_seqs, n_kv_heads, static_cast<int>(max_len), block_size, sms);
+    } else {
+        if (P < 16 || P % 16 != 0 || P % block_size != 0 || P / block_size > 2048)
+            return PKV_ERR_INVALID_ARG;
+    }
+    const long long parts = (max_len + P - 1) / P;
+    if (parts > 65535) return PKV_ERR_UNSUPPORTED;
+    plan->max_len = static_cast<int>(max_len);
+    plan->partition = P;
+    plan->max_parts = parts < 1 ? 1 : static_cast<int>(parts);
+    plan->ws_bytes = plan->max_parts > 1
+                         ? pkv::workspace_layout(num_seqs, n_q_heads, head_dim, plan->max_parts).total
+                         : 0;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                    void *k_cache, void *v_cache, int num_tokens, int n_kv_heads, int head_dim,
+                    int block_size, int64_t num_blocks, int32_t *err_word, void *cuda_stream) {
+    if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 ||
+        num_blocks <= 0 || block_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8) || (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    pkv::AppendArgs a{k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens,
+                      n_kv_heads, head_dim, block_size, num_blocks, err_word};
+    const cudaError_t e = pkv::launch_append(a, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                      int max_blocks_per_seq, int max_context_len, int partition_tokens,
+                      int *partition_tokens_out, size_t *workspace_bytes_out) {
+    Plan plan{};
+    const int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, max_context_len, partition_tokens, &plan);
+    if (rc != PKV_OK) return rc;
+    if (partition_tokens_out) *partition_tokens_out = plan.partition;
+    if (workspace_bytes_out) *workspace_bytes_out = plan.ws_bytes;
+    return PKV_OK;
+}
+
+int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           int num_seqs, int max_blocks_per_seq, int64_t num_blocks, float scale,
+                           int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                           int max_context_len, int partition_tokens, void *workspace,
+                           size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                           void *cuda_stream) {
+    if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    Plan plan{};
+    int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                       max_context_len, partition_tokens, &plan);
+    if (rc != PKV_OK) return rc;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+        (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    if (n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    pkv::DecodeArgs a{};
+    if (plan.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 16))
+            return PKV_ERR_WORKSPACE;
+        const pkv::WorkspaceLayout w =
+            pkv::workspace_layout(num_seqs, n_q_heads, head_dim, plan.max_parts);
+        char *base = static_cast<char *>(workspace);
+        a.ws_acc = reinterpret_cast<float *>(base + w.acc_offset);
+        a.ws_m = reinterpret_cast<float *>(base + w.m_offset);
+        a.ws_l = reinterpret_cast<float *>(base + w.l_offset);
+    }
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.lse_out = lse_out;
+    a.err = err_word;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.max_context_len = plan.max_len;
+    a.partition_tokens = plan.partition;
+    a.max_parts = plan.max_parts;
+    const cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
+    if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits_out) {
+    if (!err_word) return PKV_ERR_INVALID_ARG;
+    int32_t host = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (cudaMemcpyAsync(&host, err_word, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (bits_out) *bits_out = host;
+    return host == 0 ? PKV_OK : PKV_ERR_INDEX;
+}
+
+const char *paged_kv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported head_dim, block_size or group size";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA runtime error";
+        case PKV_ERR_INDEX: return "device flagged a bad index";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

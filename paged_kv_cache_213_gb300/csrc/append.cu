@@ -1,0 +1,57 @@
+// append.cu -- slot-mapped append of the new token's K/V into the block pool.
+//
+// Method: "Distributed LLM Inference Serving Platform", section 5.1: the K and
+// V vectors of a token are written directly into the physical PagedAttention
+// block assigned to it (a fresh block when the tail block is full -- the
+// caller's block manager chooses the slot; this kernel only writes).
+// One thread moves one 16-byte vector of K and one of V: coalesced along
+// head_dim, bit-exact.
+#include <cuda_fp16.h>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+__global__ void __launch_bounds__(256)
+    append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                  const int64_t *__restrict__ slots, uint4 *__restrict__ k_cache,
+                  uint4 *__restrict__ v_cache, long long total, int n_kv_heads, int chunks,
+                  int block_size, long long num_slots, int32_t *err) {
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int c = static_cast<int>(idx % chunks);
+    const long long r = idx / chunks;
+    const int j = static_cast<int>(r % n_kv_heads);
+    const long long i = r / n_kv_heads;
+    const long long s = slots[i];
+    if (s < 0) return;  // padding token
+    if (s >= num_slots) {
+        if (c == 0 && j == 0) flag_error(err, PKV_ERRBIT_SLOT);
+        return;
+    }
+    const long long block = s / block_size;
+    const long long row = s % block_size;
+    const long long dst = ((block * n_kv_heads + j) * block_size + row) * chunks + c;
+    k_cache[dst] = k_new[idx];
+    v_cache[dst] = v_new[idx];
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream) {
+    const int chunks = a.head_dim / 8;
+    const long long total = static_cast<long long>(a.num_tokens) * a.n_kv_heads * chunks;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(a.k_new), static_cast<const uint4 *>(a.v_new), a.slot_mapping,
+        static_cast<uint4 *>(a.k_cache), static_cast<uint4 *>(a.v_cache), total, a.n_kv_heads,
+        chunks, a.block_size, a.num_blocks * a.block_size, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,61 @@
+// pkv_internal.h -- launch interfaces between the C ABI layer (api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+struct AppendArgs {
+    const void *k_new;
+    const void *v_new;
+    const int64_t *slot_mapping;
+    void *k_cache;
+    void *v_cache;
+    int num_tokens;
+    int n_kv_heads;
+    int head_dim;
+    int block_size;
+    int64_t num_blocks;
+    int32_t *err;
+};
+
+struct DecodeArgs {
+    void *out;                    // fp16 [B][H][D]
+    const void *q;                // fp16 [B][H][D]
+    const void *k_cache;          // fp16 [NB][Hk][bs][D]
+    const void *v_cache;
+    const int32_t *block_tables;  // [B][MB]
+    const int32_t *context_lens;  // [B]
+    float *ws_acc;                // [B][H][max_parts][D]  unnormalised partial sums
+    float *ws_m;                  // [B][H][max_parts]     partial max (log2 units)
+    float *ws_l;                  // [B][H][max_parts]     partial sum of 2^(s - m)
+    float *lse_out;               // [B][H] or null
+    int32_t *err;                 // or null
+    int num_seqs;
+    int max_blocks_per_seq;
+    int64_t num_blocks;
+    float scale_log2;             // scale * log2(e)
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int block_size;
+    int max_context_len;          // clamp bound, > 0
+    int partition_tokens;         // multiple of 16 and of block_size
+    int max_parts;                // ceil(max_context_len / partition_tokens)
+};
+
+// Workspace carve-up shared by the planner and the launcher.
+struct WorkspaceLayout {
+    size_t acc_offset, m_offset, l_offset, total;
+};
+WorkspaceLayout workspace_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts);
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
+// Returns cudaErrorInvalidValue for a (head_dim, group) pair with no kernel.
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+bool decode_supported(int head_dim, int group);
+
+}  // namespace pkv

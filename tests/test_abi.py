@@ -1,0 +1,113 @@
+"""The C-ABI library builds for sm_103a, loads, exports every function
+include/pagedkv.h declares, and rejects bad arguments on the host (these
+calls return before any CUDA work, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_213_gb300 as pkv
+from paged_kv_cache_213_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.library()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"paged_kv_append", "paged_decode_attention", "paged_decode_plan",
+            "paged_kv_get_error", "paged_kv_status_string"} <= set(names)
+    raw = ctypes.CDLL(pkv.library_path())
+    for n in names:
+        assert hasattr(raw, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    assert pkv.status_string(0) == "ok"
+    for s in (-1, -2, -3, -4, -5):
+        assert pkv.status_string(s) not in ("ok", "unknown status")
+    assert pkv.status_string(42) == "unknown status"
+
+
+def _plan(lib, *args):
+    P = ctypes.c_int(-1)
+    W = ctypes.c_size_t(0)
+    rc = lib.paged_decode_plan(*args, ctypes.byref(P), ctypes.byref(W))
+    return rc, P.value, W.value
+
+
+def test_plan_explicit_partition(lib):
+    # B=32, H=32, Hk=8, d=128, bs=16, MB=128, max_len 2048, P=256 -> 8 partitions
+    rc, P, W = _plan(lib, 32, 32, 8, 128, 16, 128, 2048, 256)
+    assert rc == 0 and P == 256
+    rows = 32 * 32 * 8
+    up = lambda x: (x + 255) // 256 * 256
+    assert W == up(rows * 128 * 4) + 2 * up(rows * 4)
+    # one partition covers everything: no workspace
+    rc, P, W = _plan(lib, 32, 32, 8, 128, 16, 128, 256, 256)
+    assert rc == 0 and W == 0
+    # max_context_len <= 0 means MB * bs
+    rc, P, W = _plan(lib, 2, 8, 2, 64, 16, 4, 0, 16)
+    assert rc == 0 and W == up(2 * 8 * 4 * 64 * 4) + 2 * up(2 * 8 * 4 * 4)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((4, 6, 4, 128, 16, 8, 0, 64), -1),    # 6 % 4 != 0
+    ((4, 8, 2, 96, 16, 8, 0, 64), -2),     # head_dim 96 not built
+    ((4, 8, 2, 128, 12, 8, 0, 48), -2),    # block size 12
+    ((4, 48, 2, 128, 16, 8, 0, 64), -2),   # group 24
+    ((4, 8, 2, 128, 16, 8, 0, 24), -1),    # partition not a multiple of 16
+    ((4, 8, 2, 128, 32, 8, 0, 16), -1),    # partition not a multiple of the block size
+    ((4, 8, 2, 128, 1, 8, 0, 4096), -1),   # more than 2048 blocks per partition
+    ((-1, 8, 2, 128, 16, 8, 0, 64), -1),
+    ((4, 8, 2, 128, 16, 0, 0, 64), -1),
+])
+def test_plan_rejects(lib, args, status):
+    assert _plan(lib, *args)[0] == status
+
+
+def test_calls_reject_bad_arguments_without_launching(lib):
+    n = None
+    # append: zero tokens is a no-op, null pointers and odd head_dim are errors
+    assert lib.paged_kv_append(n, n, n, n, n, 0, 8, 128, 16, 10, n, n) == 0
+    assert lib.paged_kv_append(n, n, n, n, n, 4, 8, 128, 16, 10, n, n) == -1
+    assert lib.paged_kv_append(n, n, n, n, n, 4, 8, 100, 16, 10, n, n) == -1
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.paged_kv_append(fake, odd, fake, fake, fake, 4, 8, 128, 16, 10, n, n) == -1
+    # attention: null pointers, misalignment, missing workspace
+    args = dict(B=4, MB=8, NB=40, H=8, Hk=2, d=128, bs=16)
+
+    def call(out, q, kc, vc, bt, cl, mcl=0, P=64, ws=None, ws_bytes=0, scale=0.1):
+        return lib.paged_decode_attention(out, q, kc, vc, bt, cl, args["B"], args["MB"],
+                                          args["NB"], scale, args["H"], args["Hk"], args["d"],
+                                          args["bs"], mcl, P, ws, ws_bytes, n, n, n)
+    assert call(n, fake, fake, fake, fake, fake) == -1
+    assert call(odd, fake, fake, fake, fake, fake) == -1
+    assert call(fake, fake, fake, fake, fake, fake) == -3          # 2 partitions, no workspace
+    assert call(fake, fake, fake, fake, fake, fake, ws=fake, ws_bytes=64) == -3
+    assert call(fake, fake, fake, fake, fake, fake, scale=float("nan")) == -1
+    assert lib.paged_kv_get_error(n, n, n) == -1
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="a GPU is present")
+def test_auto_plan_needs_a_device(lib):
+    rc, _, _ = _plan(lib, 4, 8, 2, 128, 16, 8, 0, 0)
+    assert rc == -4

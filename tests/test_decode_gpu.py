@@ -1,0 +1,262 @@
+"""Parity of the CUDA paged decode attention (through the C ABI) with the CPU
+oracle: the five standard workloads at full size, forced split-K partition
+sizes, edge shapes, NaN-poisoned unused memory, bit-exact cases, invariances
+and device-flagged index errors."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_213_gb300 as pkv
+from gpu_util import assert_close, compare, gpu_step, oracle_step, to_dev
+from paged_kv_cache_213_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.library()
+
+
+def _sample_mask(batch, n, seed):
+    rng = np.random.default_rng(seed)
+    B, H = batch.num_seqs, batch.n_q_heads
+    mask = np.zeros((B, H), dtype=bool)
+    idx = rng.choice(B * H, size=min(n, B * H), replace=False)
+    mask.reshape(-1)[idx] = True
+    # always include the longest and the shortest sequence
+    mask[int(np.argmax(batch.context_lens)), :] = True
+    mask[int(np.argmin(batch.context_lens)), :] = True
+    return mask
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_workload_parity(cfg):
+    """Full-size workloads, poisoned, in the automatic launch configuration
+    the benchmark uses; every output (1-3) or a sample of (b, h) (4-5)."""
+    batch = wl.workload(cfg, poison=True)
+    mask = None if cfg <= 3 else _sample_mask(batch, 96, cfg)
+    g = gpu_step(batch)
+    assert g["err"] == 0
+    ref = oracle_step(batch, mask=mask)
+    assert_close(g["out"], ref["out"], mask=mask, what=f"workload {cfg}")
+    sel = mask if mask is not None else np.ones(ref["lse"].shape, dtype=bool)
+    assert np.max(np.abs(g["lse"][sel] - ref["lse"][sel])) <= 1e-4
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_append_bitexact_whole_pool(cfg):
+    batch = wl.workload(cfg, poison=True)
+    g = gpu_step(batch)
+    ref = oracle_step(batch, mask=np.zeros((batch.num_seqs, batch.n_q_heads), dtype=bool))
+    kc = g["dev"]["k_cache"].cpu().numpy().view(np.uint16)
+    vc = g["dev"]["v_cache"].cpu().numpy().view(np.uint16)
+    assert np.array_equal(kc, ref["k_cache"].view(np.uint16))
+    assert np.array_equal(vc, ref["v_cache"].view(np.uint16))
+
+
+def test_append_padding_and_bad_slot():
+    rng = np.random.default_rng(7)
+    batch = wl.make_batch("pad", [5, 16, 17, 33], 8, 2, 128, 16, rng, append=True, poison=True,
+                          append_padding=5)
+    dev = to_dev(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                        dev["v_cache"], err_word=err)
+    assert pkv.get_error(err) == 0
+    ref = oracle_step(batch, mask=np.zeros((4, 8), dtype=bool))
+    assert np.array_equal(dev["k_cache"].cpu().numpy().view(np.uint16),
+                          ref["k_cache"].view(np.uint16))
+    assert np.array_equal(dev["v_cache"].cpu().numpy().view(np.uint16),
+                          ref["v_cache"].view(np.uint16))
+    # a slot beyond the pool is flagged and skipped; everything else lands
+    before = dev["k_cache"].clone()
+    slots = dev["slot_mapping"].clone()
+    slots[0] = batch.num_blocks * batch.block_size + 3
+    pkv.paged_kv_append(dev["k_new"], dev["v_new"], slots, dev["k_cache"], dev["v_cache"],
+                        err_word=err)
+    assert pkv.get_error(err) & pkv.PKV_ERRBIT_SLOT
+    assert torch.equal(before.view(torch.int16), dev["k_cache"].view(torch.int16))
+
+
+@pytest.mark.parametrize("P", [16, 32, 64, 128, 512, 0])
+def test_forced_partitions(P):
+    """Split-K partition sizes from one tile per partition to one partition
+    per sequence: the LSE merge path and the direct path agree with the oracle."""
+    rng = np.random.default_rng(100 + P)
+    lens = [1, 15, 16, 17, 100, 255, 256, 257, 700]
+    batch = wl.make_batch("split", lens, 16, 4, 128, 16, rng, append=True, poison=True)
+    g = gpu_step(batch, partition_tokens=P)
+    assert g["err"] == 0
+    ref = oracle_step(batch)
+    assert_close(g["out"], ref["out"], what=f"P={P}")
+    assert np.max(np.abs(g["lse"] - ref["lse"])) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [1, 2, 8, 16, 32])
+def test_edge_shapes(d, g, bs):
+    rng = np.random.default_rng(1000 * d + 10 * g + bs)
+    Hk = 2
+    lens = [1, 2, 15, 16, 17, 31, 33, 64, 130]
+    batch = wl.make_batch("edge", lens, Hk * g, Hk, d, bs, rng, append=True, poison=True)
+    for P in (0, max(16, bs)):
+        out = gpu_step(batch, partition_tokens=P)
+        assert out["err"] == 0
+        ref = oracle_step(batch)
+        assert_close(out["out"], ref["out"], what=f"d={d} g={g} bs={bs} P={P}")
+
+
+def test_empty_sequences():
+    rng = np.random.default_rng(3)
+    batch = wl.make_batch("empty", [0, 5, 0, 40], 8, 2, 128, 16, rng, append=False, poison=True,
+                          max_blocks_per_seq=4)
+    for P in (0, 16):
+        g = gpu_step(batch, partition_tokens=P)
+        assert g["err"] == 0
+        assert np.all(g["out"][[0, 2]] == 0)
+        assert np.all(np.isneginf(g["lse"][[0, 2]]))
+        ref = oracle_step(batch)
+        assert_close(g["out"], ref["out"], what="empty")
+
+
+def test_single_token_is_bitexact():
+    """L = 1: the softmax weight is exactly 1, so out == V_0 bit for bit."""
+    rng = np.random.default_rng(4)
+    batch = wl.make_batch("one", [1] * 12, 32, 8, 128, 16, rng, append=True, poison=True)
+    g = gpu_step(batch)
+    ref = oracle_step(batch)
+    assert np.array_equal(g["out"].view(np.uint16), ref["out16"].view(np.uint16))
+    # and the value is the appended V row
+    vn = batch.v_new.astype(np.float16)
+    for b in range(12):
+        for h in range(32):
+            assert np.array_equal(g["out"][b, h].view(np.uint16), vn[b, h // 4].view(np.uint16))
+
+
+def test_dominant_logit_gathers_exact_row():
+    """A huge scale makes the softmax one-hot on the arg-max token: the output
+    is that token's V row bit for bit -- the gather through the block table
+    picks exactly the oracle's row, across partitions."""
+    rng = np.random.default_rng(5)
+    lens = [40, 300, 1000, 77]
+    batch = wl.make_batch("onehot", lens, 8, 2, 128, 16, rng, scale=4000.0, append=True,
+                          poison=True)
+    ref = oracle_step(batch)
+    # logits in double from the appended cache, to find clear winners
+    kc = ref["k_cache"].astype(np.float64)
+    checked = 0
+    for P in (0, 64):
+        g = gpu_step(batch, partition_tokens=P)
+        assert g["err"] == 0
+        for b, L in enumerate(lens):
+            t = np.arange(L)
+            rows = kc[batch.block_tables[b, t // 16], :, t % 16, :]  # [L, Hk, d]
+            for h in range(8):
+                s = rows[:, h // 4, :] @ batch.q[b, h].astype(np.float64)
+                top2 = np.sort(s)[-2:]
+                if top2[1] - top2[0] < 0.05:
+                    continue
+                assert np.array_equal(g["out"][b, h].view(np.uint16),
+                                      ref["out16"][b, h].view(np.uint16))
+                checked += 1
+    assert checked > 20
+
+
+def test_invariances_are_bitwise():
+    """Physical block order, block size 1 vs 16 and shared vs copied prefix
+    blocks do not change a single output bit (the kernel sums in logical
+    order whatever the addresses)."""
+    rng = np.random.default_rng(6)
+    lens = [70, 16, 530, 33]
+    base = wl.make_batch("inv", lens, 16, 4, 128, 16, rng, append=False, poison=True)
+    out0 = gpu_step(base, partition_tokens=64)["out"]
+
+    def relayout(bs, seed, shared=None):
+        r = np.random.default_rng(seed)
+        b2 = wl.make_batch("inv2", lens, 16, 4, 128, bs, r, append=False, poison=True,
+                           shared=shared)
+        b2.q = base.q
+        # copy the logical K/V of `base` into the new layout
+        for b, L in enumerate(lens):
+            t = np.arange(L)
+            src_k = base.k_cache[base.block_tables[b, t // 16], :, t % 16, :]
+            src_v = base.v_cache[base.block_tables[b, t // 16], :, t % 16, :]
+            b2.k_cache[b2.block_tables[b, t // bs], :, t % bs, :] = src_k
+            b2.v_cache[b2.block_tables[b, t // bs], :, t % bs, :] = src_v
+        return b2
+
+    for bs, seed in ((16, 60), (1, 61), (8, 62)):
+        out = gpu_step(relayout(bs, seed), partition_tokens=64)["out"]
+        assert np.array_equal(out.view(np.uint16), out0.view(np.uint16)), f"bs={bs}"
+    # shared prefix: make the first 32 tokens of sequences 0 and 2 identical
+    base.k_cache[base.block_tables[2, :2]] = base.k_cache[base.block_tables[0, :2]]
+    base.v_cache[base.block_tables[2, :2]] = base.v_cache[base.block_tables[0, :2]]
+    copied = gpu_step(base, partition_tokens=64)["out"]
+    shared = relayout(16, 63, shared=[([0, 2], 2)])
+    assert shared.block_tables[0, 0] == shared.block_tables[2, 0]
+    out = gpu_step(shared, partition_tokens=64)["out"]
+    assert np.array_equal(out.view(np.uint16), copied.view(np.uint16))
+
+
+def test_bad_block_id_and_length_are_flagged():
+    rng = np.random.default_rng(8)
+    batch = wl.make_batch("bad", [40, 20], 8, 2, 128, 16, rng, append=False, poison=False)
+    batch.block_tables[0, 1] = batch.num_blocks + 5
+    g = gpu_step(batch)
+    assert g["err"] & pkv.PKV_ERRBIT_BLOCK_ID
+    ok = oracle_step(batch, mask=np.array([[False] * 8, [True] * 8]))
+    assert_close(g["out"][1], ok["out"][1], what="untouched sequence")
+    batch = wl.make_batch("bad", [40, 20], 8, 2, 128, 16, rng, append=False, poison=False)
+    batch.context_lens[1] = batch.max_blocks_per_seq * 16 + 1
+    g = gpu_step(batch, max_context_len=0)
+    assert g["err"] & pkv.PKV_ERRBIT_CONTEXT
+
+
+def test_host_side_errors():
+    rng = np.random.default_rng(9)
+    batch = wl.make_batch("h", [300], 8, 2, 128, 16, rng, append=False, poison=False)
+    dev = to_dev(batch)
+    P, ws = pkv.decode_plan(1, 8, 2, 128, 16, batch.max_blocks_per_seq, 300, 64)
+    assert P == 64 and ws > 0
+    small = torch.empty(ws - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["context_lens"], 0.1, 8, 2, 128, 16, max_context_len=300,
+                                   partition_tokens=64, workspace=small)
+    assert e.value.status == -3
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["context_lens"], 0.1, 8, 2, 128, 16, partition_tokens=24)
+
+
+def test_side_stream_and_reuse():
+    """Works on a non-default stream and with a caller-owned workspace reused
+    across calls."""
+    batch = wl.workload(1, poison=True)
+    ref = oracle_step(batch)
+    dev = to_dev(batch)
+    s = torch.cuda.Stream()
+    P, ws = pkv.decode_plan(batch.num_seqs, 4, 2, 64, 16, batch.max_blocks_per_seq,
+                            batch.max_context_len, 16)
+    work = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                            dev["v_cache"])
+        outs = [pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                           dev["block_tables"], dev["context_lens"], batch.scale,
+                                           4, 2, 64, 16, max_context_len=batch.max_context_len,
+                                           partition_tokens=16, workspace=work)
+                for _ in range(3)]
+    s.synchronize()
+    for o in outs:
+        assert_close(o.cpu().numpy(), ref["out"], what="side stream")
+    assert np.array_equal(outs[0].cpu().numpy().view(np.uint16),
+                          outs[2].cpu().numpy().view(np.uint16))
+    assert math.isfinite(float(compare(outs[1].cpu().numpy(), ref["out"])[0]))
