@@ -42,7 +42,8 @@
  *
  * Ownership: every pointer is a device pointer the caller allocates and owns
  * (except where a host pointer is stated).  The library allocates no memory
- * and keeps no state besides a cached per-device attribute lookup.  Tensor
+ * and keeps no state besides a cached per-device attribute lookup (and the
+ * static scratch array of paged_decode_attention_noalloc).  Tensor
  * pointers (q, out, caches, k_new, v_new) must be 16-byte aligned.
  *
  * Errors: a call that detects a bad argument on the host returns a negative
@@ -157,6 +158,40 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int block_size, int max_context_len, int partition_tokens,
                            void *workspace, size_t workspace_bytes, float *lse_out,
                            int32_t *err_word, void *cuda_stream);
+
+/*
+ * Allocation-free variant of paged_decode_attention.  The pages have no
+ * counterpart to this call.  It serves callers that cannot allocate device
+ * memory and so cannot supply the split-K workspace: an operator running
+ * inside a host framework's plugin interface that is handed its input and
+ * output tensors but no allocator, or a foreign-language binding without
+ * access to a CUDA allocator.
+ *
+ * Same arguments and results as paged_decode_attention, without workspace
+ * and workspace_bytes.  The split-K partial results go to a static device
+ * array of PKV_NOALLOC_SCRATCH_BYTES bytes inside the library, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *  - Returns PKV_ERR_WORKSPACE, launching nothing, when the problem's split
+ *    needs more than PKV_NOALLOC_SCRATCH_BYTES (paged_decode_plan reports the
+ *    need; a larger partition_tokens lowers it).
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture on that device.
+ *  - All calls share the one array, and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero: each call writes every partial
+ *    result it reads.  Calls whose kernels overlap in time on the GPU (on
+ *    different streams, or from different host threads) race on the array
+ *    and give wrong results; serialise them.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+int paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs,
+                                   int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                   int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                   int max_context_len, int partition_tokens, float *lse_out,
+                                   int32_t *err_word, void *cuda_stream);
 
 /*
  * Reads the device error word: waits for cuda_stream, copies *err_word to the

@@ -203,6 +203,49 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   n_q_heads, n_kv_heads, head_dim, block_size,
+                                   max_context_len=None, partition_tokens=0, out=None, lse=None,
+                                   err_word=None):
+    """Like paged_decode_attention, but the split-K scratch is the library's
+    static device array, for callers that cannot allocate device memory.
+    ``out`` (and ``lse``) should be passed in by such callers; calls whose
+    kernels overlap on the GPU race on the shared scratch."""
+    lib = library()
+    fn = lib.paged_decode_attention_noalloc
+    if fn.restype is not ctypes.c_int:
+        c = ctypes
+        p = c.c_void_p
+        fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float, c.c_int,
+                       c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, p, p]
+        fn.restype = c.c_int
+    dev = q.device
+    for t, name, dt in ((q, "q", torch.float16), (k_cache, "k_cache", torch.float16),
+                        (v_cache, "v_cache", torch.float16),
+                        (block_tables, "block_tables", torch.int32),
+                        (context_lens, "context_lens", torch.int32)):
+        _need(t, name, dt, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    B, MB = block_tables.shape
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), n_q_heads, n_kv_heads,
+                head_dim, block_size, mcl, int(partition_tokens), _ptr(lse), _ptr(err_word),
+                _stream_handle(dev))
+    _check("paged_decode_attention_noalloc", rc)
+    return out
+
+
 def get_error(err_word: torch.Tensor) -> int:
     """Wait for the current stream and return the device error word's bits."""
     _need(err_word, "err_word", torch.int32)
