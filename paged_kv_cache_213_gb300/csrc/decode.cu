@@ -13,6 +13,9 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include "pagedkv.h"
 #include "pkv_internal.h"
@@ -377,7 +380,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const DecodeArgs a) {
 }
 
 template <int D, int G>
-cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
+cudaError_t launch_simt_t(const DecodeArgs &a, cudaStream_t stream) {
     using C = Cfg<D, G>;
     const int ids = (a.partition_tokens / a.block_size + 3) / 4 * 4;
     const size_t smem = C::UNION_BYTES + static_cast<size_t>(ids) * 4;
@@ -389,25 +392,13 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
     }
     dim3 grid(a.num_seqs, a.n_kv_heads, a.max_parts);
     kern<<<grid, kThreads, smem, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || a.max_parts <= 1) return e;
-    const long long warps = static_cast<long long>(a.num_seqs) * a.n_q_heads;
-    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    lse_merge_kernel<D><<<blocks, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-bool decode_supported(int head_dim, int group) {
-    return (head_dim == 64 || head_dim == 128) &&
-           (group == 1 || group == 2 || group == 4 || group == 8);
-}
-
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
+cudaError_t launch_simt(const DecodeArgs &a, cudaStream_t stream) {
     const int g = a.n_q_heads / a.n_kv_heads;
 #define PKV_CASE(D_, G_) \
-    if (a.head_dim == D_ && g == G_) return launch_decode_t<D_, G_>(a, stream);
+    if (a.head_dim == D_ && g == G_) return launch_simt_t<D_, G_>(a, stream);
     PKV_CASE(128, 1)
     PKV_CASE(128, 2)
     PKV_CASE(128, 4)
@@ -418,6 +409,47 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     PKV_CASE(64, 8)
 #undef PKV_CASE
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const DecodeArgs &a, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(a.num_seqs) * a.n_q_heads;
+    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+    if (a.head_dim == 128)
+        lse_merge_kernel<128><<<blocks, 256, 0, stream>>>(a);
+    else
+        lse_merge_kernel<64><<<blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// Kernel choice: the tensor-core kernel whenever it applies (block size a
+// multiple of 16); PKV_DECODE_KERNEL=simt or =mma in the environment forces
+// one (read once per process).
+int kernel_override() {
+    static std::once_flag once;
+    static int mode = 0;
+    std::call_once(once, [] {
+        const char *e = std::getenv("PKV_DECODE_KERNEL");
+        if (e && std::strcmp(e, "simt") == 0) mode = 1;
+        if (e && std::strcmp(e, "mma") == 0) mode = 2;
+    });
+    return mode;
+}
+
+}  // namespace
+
+bool decode_supported(int head_dim, int group) {
+    return (head_dim == 64 || head_dim == 128) &&
+           (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
+    const int mode = kernel_override();
+    const bool mma_ok = decode_mma_supported(a);
+    if (mode == 2 && !mma_ok) return cudaErrorInvalidValue;
+    const cudaError_t e =
+        (mma_ok && mode != 1) ? launch_decode_mma(a, stream) : launch_simt(a, stream);
+    if (e != cudaSuccess || a.max_parts <= 1) return e;
+    return launch_merge(a, stream);
 }
 
 WorkspaceLayout workspace_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts) {

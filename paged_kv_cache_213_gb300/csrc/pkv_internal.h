@@ -57,5 +57,8 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
 // Returns cudaErrorInvalidValue for a (head_dim, group) pair with no kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 bool decode_supported(int head_dim, int group);
+// Tensor-core kernel (decode_mma.cu): partition pass only, no merge.
+bool decode_mma_supported(const DecodeArgs &a);
+cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t stream);
 
 }  // namespace pkv

@@ -79,3 +79,22 @@ def assert_close(gpu_out16, ref64, mask=None, what=""):
                               else np.asarray(gpu_out16, dtype=np.float64))), f"{what}: non-finite"
     assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs={max_abs:.3e} rel={rel:.3e}"
     return max_abs, rel
+
+
+def relayout(base, bs, seed, shared=None):
+    """The same logical K/V (and q) as `base` (attention-only batch) in a new
+    pool: block size `bs`, a fresh random physical order, optional sharing."""
+    from paged_kv_cache_213_gb300 import workloads as wl
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in base.context_lens]
+    b2 = wl.make_batch("relayout", lens, base.n_q_heads, base.n_kv_heads, base.head_dim, bs,
+                       rng, scale=base.scale, append=False, poison=True, shared=shared)
+    b2.q = base.q
+    bs0 = base.block_size
+    for b, L in enumerate(lens):
+        t = np.arange(L)
+        src_k = base.k_cache[base.block_tables[b, t // bs0], :, t % bs0, :]
+        src_v = base.v_cache[base.block_tables[b, t // bs0], :, t % bs0, :]
+        b2.k_cache[b2.block_tables[b, t // bs], :, t % bs, :] = src_k
+        b2.v_cache[b2.block_tables[b, t // bs], :, t % bs, :] = src_v
+    return b2
