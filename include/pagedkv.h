@@ -106,14 +106,20 @@ int paged_kv_append(const void *k_new, const void *v_new, const int64_t *slot_ma
 /*
  * Split planning for paged_decode_attention (host only; no device work).
  * partition_tokens = 0 asks for the automatic choice, which depends on the
- * current device's SM count (a CUDA query; fails with PKV_ERR_CUDA when no
- * device is present).  A nonzero partition_tokens is checked and echoed:
- * it must be a positive multiple of 16 and of block_size with
- * partition_tokens / block_size <= 2048.
+ * current device (SM count and occupancy; a CUDA query that fails with
+ * PKV_ERR_CUDA when no device is present).  For block sizes that are a
+ * multiple of 16 and up to 2048 sequences the automatic choice is the
+ * balanced split: the (sequence, KV head, 16-token tile) work units are cut
+ * into equal contiguous ranges, one per warp of a grid that fills the GPU
+ * once, and segments cut by a range boundary are merged by log-sum-exp.
+ * Otherwise it is a fixed partition size.  A nonzero partition_tokens selects
+ * fixed partitions of that many tokens and is checked and echoed: a positive
+ * multiple of 16 and of block_size with partition_tokens / block_size <= 2048.
  *  max_context_len <= 0 means max_blocks_per_seq * block_size.
- *  *partition_tokens_out  (host, may be NULL) tokens per split-K partition
+ *  *partition_tokens_out  (host, may be NULL) tokens per fixed partition, or
+ *                         0 for the balanced split
  *  *workspace_bytes_out   (host, may be NULL) workspace the call needs; 0 when
- *                         every sequence fits one partition
+ *                         every sequence fits one fixed partition
  */
 int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                       int block_size, int max_blocks_per_seq, int max_context_len,
@@ -129,8 +135,9 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
  * with K_t, V_t the rows of KV head h / (n_q_heads / n_kv_heads) gathered
  * through block_tables[b].  Logits and the softmax run in fp32 (online
  * max/sum rescaling); the output is rounded to fp16 (round to nearest even).
- * Long contexts are split into partitions of partition_tokens tokens whose
- * partial results are merged by log-sum-exp (flash-decoding split).
+ * Long contexts are split (balanced split or fixed partitions, see
+ * paged_decode_plan) and the partial results merged by log-sum-exp
+ * (flash-decoding split).
  * L_b = 0 gives out = 0 and lse = -inf.
  *
  *  out            device fp16 [num_seqs][n_q_heads][head_dim]
@@ -142,7 +149,7 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
  *  max_context_len an upper bound on every context length (no device sync
  *                 is needed to know it); <= 0 means max_blocks_per_seq*block_size
  *  partition_tokens 0 = automatic (see paged_decode_plan)
- *  workspace      device scratch of at least the planned bytes (16-byte
+ *  workspace      device scratch of at least the planned bytes (256-byte
  *                 aligned), may be NULL when the plan needs 0 bytes; the
  *                 caller owns it; calls that overlap in time need separate
  *                 workspaces

@@ -22,6 +22,8 @@ LIB_PATH = os.path.join(OUT_DIR, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+# extra nvcc flags (e.g. -D tuning macros) from the environment
+NVCC_FLAGS += os.environ.get("PKV_NVCC_FLAGS", "").split()
 
 
 def nvcc() -> str:

@@ -59,9 +59,11 @@ int auto_partition(int num_seqs, int n_kv_heads, int max_len, int block_size, in
 
 struct Plan {
     int max_len;
-    int partition;
+    int partition;   // 0: the balanced kernel (no fixed partitions)
     int max_parts;
     size_t ws_bytes;
+    bool balanced;
+    pkv::BalancedPlan bal;
 };
 
 int make_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
@@ -77,6 +79,21 @@ int make_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int blo
     long long max_len = max_context_len <= 0 ? cap : max_context_len;
     if (max_len > cap) max_len = cap;
     int P = partition_tokens;
+    const int group = n_q_heads / n_kv_heads;
+    if (P == 0 && pkv::kernel_override() == 0 &&
+        pkv::balanced_supported(num_seqs, head_dim, group, block_size, 0)) {
+        // work split evenly over warps; the grid and workspace follow the device
+        if (!pkv::balanced_plan(num_seqs, n_q_heads, n_kv_heads, head_dim,
+                                static_cast<int>(max_len), &plan->bal))
+            return PKV_ERR_CUDA;
+        plan->balanced = true;
+        plan->max_len = static_cast<int>(max_len);
+        plan->partition = 0;
+        plan->max_parts = 1;
+        plan->ws_bytes = plan->bal.ws_bytes;
+        return PKV_OK;
+    }
+    plan->balanced = false;
     if (P == 0) {
         int sms = 0;
         const int rc = sm_count(&sms);
@@ -151,9 +168,12 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
         return PKV_ERR_INVALID_ARG;
     if (n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
     pkv::DecodeArgs a{};
-    if (plan.ws_bytes > 0) {
-        if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 16))
-            return PKV_ERR_WORKSPACE;
+    if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes ||
+                              !aligned(workspace, 256)))
+        return PKV_ERR_WORKSPACE;
+    if (plan.balanced) {
+        a.ws_acc = static_cast<float *>(workspace);  // base of the balanced layout
+    } else if (plan.ws_bytes > 0) {
         const pkv::WorkspaceLayout w =
             pkv::workspace_layout(num_seqs, n_q_heads, head_dim, plan.max_parts);
         char *base = static_cast<char *>(workspace);
@@ -180,7 +200,13 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
     a.max_context_len = plan.max_len;
     a.partition_tokens = plan.partition;
     a.max_parts = plan.max_parts;
-    const cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
+    if (plan.balanced &&
+        static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
+        return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+    const cudaError_t e =
+        plan.balanced
+            ? pkv::launch_decode_balanced(a, plan.bal, static_cast<cudaStream_t>(cuda_stream))
+            : pkv::launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256)
                   const int64_t *__restrict__ slots, uint4 *__restrict__ k_cache,
                   uint4 *__restrict__ v_cache, long long total, int n_kv_heads, int chunks,
                   int block_size, long long num_slots, int32_t *err) {
+    allow_dependent_launch();  // the attention kernel may get scheduled meanwhile
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const int c = static_cast<int>(idx % chunks);

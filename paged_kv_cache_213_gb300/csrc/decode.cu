@@ -421,9 +421,11 @@ cudaError_t launch_merge(const DecodeArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+}  // namespace
+
 // Kernel choice: the tensor-core kernel whenever it applies (block size a
 // multiple of 16); PKV_DECODE_KERNEL=simt or =mma in the environment forces
-// one (read once per process).
+// one of the partition-grid kernels (read once per process).
 int kernel_override() {
     static std::once_flag once;
     static int mode = 0;
@@ -434,8 +436,6 @@ int kernel_override() {
     });
     return mode;
 }
-
-}  // namespace
 
 bool decode_supported(int head_dim, int group) {
     return (head_dim == 64 || head_dim == 128) &&

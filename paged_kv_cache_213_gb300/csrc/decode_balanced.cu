@@ -1,0 +1,523 @@
+// decode_balanced.cu -- paged decode attention with the work split evenly
+// over warps (the default tensor-core path).
+//
+// The work of one call is the list of (sequence b, KV head j, 16-token tile t)
+// units, ordered b, then j, then t: T units in all.  Each of the W warps of
+// the grid (W = 4 x number of CTAs, sized to fill every SM once) takes the
+// contiguous range [w*T/W, (w+1)*T/W), so every warp moves the same number of
+// K/V bytes (+-1 tile) whatever the mix of context lengths.  A warp streams
+// its range through its own 2-stage ring of TMA-loaded tiles, carrying the
+// online-softmax state of the current (b, j) "segment".  When a segment ends
+// inside the range the warp writes the final output; a segment cut by a range
+// boundary leaves a partial result (m, l, acc) in one of the warp's two
+// workspace slots, and a second kernel merges those by log-sum-exp.
+//
+// Method: "Distributed LLM Inference Serving Platform", sections 2-3 (block
+// table gather) and 5.1 (attention over every block of a sequence's table),
+// GQA from section 1; online softmax and the log-sum-exp combination of
+// partial results from FlashAttention-2 (section 14 references).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "mma_tile.cuh"
+#include "pagedkv.h"
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kW = 4;  // warps per CTA, each an independent worker
+#ifndef PKV_BAL_STAGES
+#define PKV_BAL_STAGES 2
+#endif
+constexpr int kS = PKV_BAL_STAGES;  // ring stages per warp
+constexpr int kThreadsB = kW * 32;
+constexpr int kMaxSeqsBalanced = 2048;
+constexpr float kLn2b = 0.69314718055994531f;
+
+template <int D, int G>
+struct BalCfg : MmaCfg<D> {
+    static constexpr int Q_BYTES = G * D * 2;                      // the group's query rows
+    static constexpr int SLOT_BYTES = 2 * MmaCfg<D>::TILE_BYTES;   // K tile, V tile
+    static constexpr int PIPE_BYTES = kW * kS * SLOT_BYTES;
+    static constexpr int QS_BYTES = kW * kS * Q_BYTES;
+};
+
+// Workspace: int pre[B+1] (tile prefix over sequences), then per worker two
+// piece slots: acc [W][2][G][D], m [W][2][G], l [W][2][G] (fp32).
+struct BalLayout {
+    size_t pre, acc, m, l, total;
+};
+__host__ __device__ inline BalLayout bal_layout(int B, int workers, int G, int D) {
+    BalLayout L{};
+    const size_t slots = static_cast<size_t>(workers) * 2 * G;
+    L.pre = 0;
+    L.acc = ((static_cast<size_t>(B) + 1) * 4 + 255) / 256 * 256;
+    L.m = L.acc + (slots * D * 4 + 255) / 256 * 256;
+    L.l = L.m + (slots * 4 + 255) / 256 * 256;
+    L.total = L.l + (slots * 4 + 255) / 256 * 256;
+    return L;
+}
+
+__device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b, bool flag) {
+    const int L = a.context_lens[b];
+    const long long cap_ll = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+    const int cap = static_cast<int>(cap_ll < a.max_context_len ? cap_ll : a.max_context_len);
+    if (L < 0 || L > cap) {
+        if (flag) flag_error(a.err, PKV_ERRBIT_CONTEXT);
+        return L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+// Position of unit x: the sequence b whose units contain it, the KV head j,
+// the tile t.  pre[] is the tile prefix (units of b: Hk * pre[b] ..).
+struct Cursor {
+    int b, j, t;
+};
+
+__device__ __forceinline__ Cursor locate(long long x, const int *pre, int B, int Hk) {
+    int lo = 0, hi = B - 1;  // largest b with Hk * pre[b] <= x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<long long>(Hk) * pre[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int r = static_cast<int>(x - static_cast<long long>(Hk) * pre[lo]);  // < Hk * nt
+    const int nt = pre[lo + 1] - pre[lo];
+    return Cursor{lo, r / nt, r % nt};
+}
+
+__device__ __forceinline__ void advance(Cursor &c, const int *pre, int B, int Hk) {
+    if (++c.t < pre[c.b + 1] - pre[c.b]) return;
+    c.t = 0;
+    if (++c.j < Hk) return;
+    c.j = 0;
+    do {
+        ++c.b;
+    } while (c.b < B && pre[c.b + 1] == pre[c.b]);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreadsB)
+    decode_balanced_kernel(const __grid_constant__ DecodeArgs a,
+                           const __grid_constant__ CUtensorMap tmap_k,
+                           const __grid_constant__ CUtensorMap tmap_v, const int workers) {
+    using C = BalCfg<D, G>;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint64_t full_bar[kW][kS];
+    __shared__ int s_ok[kW][kS];
+    __shared__ int s_scan[kW];
+    const uint32_t raw_s = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+    unsigned char *qslots = smem + C::PIPE_BYTES;
+    int *s_pre = reinterpret_cast<int *>(qslots + C::QS_BYTES);  // [B + 1]
+    int *s_len = s_pre + a.num_seqs + 1;                          // [B]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    const int B = a.num_seqs;
+    const int H = a.n_q_heads;
+    const int Hk = a.n_kv_heads;
+    const int bs = a.block_size;
+    const BalLayout lay = bal_layout(B, workers, G, D);
+    char *ws = reinterpret_cast<char *>(a.ws_acc);
+    grid_dependency_wait();    // the previous kernel (e.g. the append) is done
+    allow_dependent_launch();  // the merge kernel may get scheduled meanwhile
+
+    // --- tile prefix over sequences: contiguous chunk per thread, then a scan
+    const int chunk = (B + kThreadsB - 1) / kThreadsB;
+    const int c0 = min(B, tid * chunk);
+    const int c1 = min(B, c0 + chunk);
+    int local = 0;
+    for (int b = c0; b < c1; ++b) {
+        const int L = clamped_len(a, b, blockIdx.x == 0);
+        s_len[b] = L;
+        local += (L + kMmaTile - 1) / kMmaTile;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    if (tid == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+        for (int w = 0; w < kW; ++w)
+            for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_scan[w];
+    int run = base + incl - local;
+    for (int b = c0; b < c1; ++b) {
+        s_pre[b] = run;
+        run += (s_len[b] + kMmaTile - 1) / kMmaTile;
+    }
+    if (tid == kThreadsB - 1) s_pre[B] = base + incl;
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int b = tid; b <= B; b += kThreadsB) reinterpret_cast<int *>(ws + lay.pre)[b] = s_pre[b];
+
+    // --- this warp's range of units
+    const int w = blockIdx.x * kW + warp;
+    const long long T = static_cast<long long>(Hk) * s_pre[B];
+    const long long w0 = w * T / workers;
+    const long long w1 = (w + 1) * T / workers;
+    const int n = static_cast<int>(w1 - w0);
+    if (n <= 0) {  // more warps than units: mark the slot the merge may visit as empty
+        if (g < G && tq == 0)
+            reinterpret_cast<float *>(ws + lay.m)[(static_cast<size_t>(w) * 2) * G + g] = -INFINITY;
+        return;  // no further CTA-wide barriers below
+    }
+
+    unsigned char *my_pipe = smem + warp * kS * C::SLOT_BYTES;
+    unsigned char *my_q = qslots + warp * kS * C::Q_BYTES;
+    Cursor pc = locate(w0, s_pre, B, Hk);  // producer cursor
+    Cursor cc = pc;                        // consumer cursor
+    int prev_seg_p = -1;
+
+    // Block ids of the range, 32 tiles at a time: lane i holds the id of tile
+    // 32c + i, for the chunk c being issued (ids_cur) and the next (ids_next),
+    // so no table load sits on the issue path.
+    auto load_ids = [&](int chunk) -> int {
+        const int kk = chunk * 32 + lane;
+        if (kk >= n) return -1;
+        const Cursor c = locate(w0 + kk, s_pre, B, Hk);
+        return a.block_tables[static_cast<size_t>(c.b) * a.max_blocks_per_seq +
+                              (c.t * kMmaTile) / bs];
+    };
+    int ids_cur = load_ids(0);
+    int ids_next = load_ids(1);
+
+    // All lanes call (the cursor bookkeeping is warp-uniform); lane 0 issues.
+    auto issue = [&](int k) {
+        const int slot = k % kS;
+        const int seg = pc.b * Hk + pc.j;
+        const bool newseg = seg != prev_seg_p;
+        prev_seg_p = seg;
+        if (k > 0 && (k & 31) == 0) {
+            ids_cur = ids_next;
+            ids_next = load_ids((k >> 5) + 1);
+        }
+        const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
+        if (lane == 0) {
+            uint64_t *bar = &full_bar[warp][slot];
+            const int tok0 = pc.t * kMmaTile;
+            const bool ok = id >= 0 && id < a.num_blocks;
+            if (!ok) flag_error(a.err, PKV_ERRBIT_BLOCK_ID);
+            s_ok[warp][slot] = ok;
+            const uint32_t bytes = (ok ? 2 * C::TILE_BYTES : 0) + (newseg ? C::Q_BYTES : 0);
+            mbar_arrive_expect_tx(bar, bytes);
+            if (ok) {
+                unsigned char *kdst = my_pipe + slot * C::SLOT_BYTES;
+                unsigned char *vdst = kdst + C::TILE_BYTES;
+                const int row = (id * Hk + pc.j) * bs + (tok0 % bs);
+#pragma unroll
+                for (int bx = 0; bx < C::BOXES; ++bx) {
+                    tma_load_2d(kdst + bx * C::BOX_BYTES, &tmap_k, bx * 64, row, bar);
+                    tma_load_2d(vdst + bx * C::BOX_BYTES, &tmap_v, bx * 64, row, bar);
+                }
+            }
+            if (newseg)
+                bulk_copy_g2s(my_q + slot * C::Q_BYTES,
+                              static_cast<const __half *>(a.q) +
+                                  (static_cast<size_t>(pc.b) * H + static_cast<size_t>(pc.j) * G) * D,
+                              C::Q_BYTES, bar);
+        }
+        advance(pc, s_pre, B, Hk);
+    };
+
+    const int pro = n < kS ? n : kS;
+    for (int k = 0; k < pro; ++k) issue(k);
+    int issued = pro;
+
+    float o[C::NB_D][4];
+    uint32_t qa[C::NP][4];
+    float m_run = -INFINITY, l_run = 0.f;
+    int cur_seg = -1, pb = 0, pj = 0, piece_t0 = 0, last_t = 0, piece_no = 0;
+
+    // Writes the finished piece [piece_t0, last_t] of segment (pb, pj).
+    auto flush = [&]() {
+        float lt = l_run;
+        lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+        const int nt = s_pre[pb + 1] - s_pre[pb];
+        const bool complete = piece_t0 == 0 && last_t == nt - 1;
+        if (g < G) {
+            const size_t bh = static_cast<size_t>(pb) * H + static_cast<size_t>(pj) * G + g;
+            if (complete) {
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
+#pragma unroll
+                for (int nb = 0; nb < C::NB_D; ++nb)
+                    dst[nb * 4 + tq] = __floats2half2_rn(o[nb][0] * inv, o[nb][1] * inv);
+                if (tq == 0 && a.lse_out)
+                    a.lse_out[bh] = lt > 0.f ? (m_run + log2f(lt)) * kLn2b : -INFINITY;
+            } else {
+                const size_t pi = (static_cast<size_t>(w) * 2 + (piece_no == 0 ? 0 : 1)) * G + g;
+                float2 *acc = reinterpret_cast<float2 *>(ws + lay.acc) + pi * (D / 2);
+#pragma unroll
+                for (int nb = 0; nb < C::NB_D; ++nb) acc[nb * 4 + tq] = make_float2(o[nb][0], o[nb][1]);
+                if (tq == 0) {
+                    reinterpret_cast<float *>(ws + lay.m)[pi] = m_run;
+                    reinterpret_cast<float *>(ws + lay.l)[pi] = lt;
+                }
+            }
+        }
+        ++piece_no;
+    };
+
+    int k = 0;
+    bool timed_out = false;
+    for (; k < n; ++k) {
+        const int slot = k % kS;
+        const bool ok = mbar_wait_bounded(&full_bar[warp][slot], (k / kS) & 1);
+        if (__any_sync(0xffffffffu, !ok)) {
+            timed_out = true;
+            break;
+        }
+        const int seg = cc.b * Hk + cc.j;
+        if (seg != cur_seg) {
+            if (cur_seg >= 0) flush();
+#pragma unroll
+            for (int nb = 0; nb < C::NB_D; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
+            load_q_frag<D>(qa, reinterpret_cast<const __half *>(my_q + slot * C::Q_BYTES) +
+                                   (g < G ? g : 0) * D,
+                           g < G, tq);
+            cur_seg = seg;
+            pb = cc.b;
+            pj = cc.j;
+            piece_t0 = cc.t;
+        }
+        last_t = cc.t;
+        unsigned char *ks = my_pipe + slot * C::SLOT_BYTES;
+        unsigned char *vs = ks + C::TILE_BYTES;
+        const int n_valid = s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - cc.t * kMmaTile) : 0;
+        mma_tile<D>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
+        __syncwarp();
+        if (k + kS < n) {
+            issue(k + kS);
+            ++issued;
+        }
+        advance(cc, s_pre, B, Hk);
+    }
+    if (timed_out) {
+        if (lane == 0) {
+            flag_error(a.err, PKV_ERRBIT_TIMEOUT);
+            for (int kk = k; kk < issued; ++kk)
+                mbar_wait_bounded(&full_bar[warp][kk % kS], (kk / kS) & 1);
+        }
+        return;
+    }
+    if (cur_seg >= 0) flush();
+}
+
+// One warp per (sequence, query head): segments cut over several workers are
+// merged by log-sum-exp; empty sequences get out = 0, lse = -inf.
+template <int D, int G>
+__global__ void __launch_bounds__(256)
+    balanced_merge_kernel(const __grid_constant__ DecodeArgs a, const int workers) {
+    constexpr int E = D / 32;
+    const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) / 32);
+    const int lane = threadIdx.x % 32;
+    const int B = a.num_seqs;
+    const int H = a.n_q_heads;
+    const int Hk = a.n_kv_heads;
+    grid_dependency_wait();  // the decode kernel's partial results are visible
+    if (warp >= B * H) return;
+    const int b = warp / H;
+    const int h = warp % H;
+    const int j = h / G;
+    const int gi = h % G;
+    const BalLayout lay = bal_layout(B, workers, G, D);
+    const char *ws = reinterpret_cast<const char *>(a.ws_acc);
+    const int *pre = reinterpret_cast<const int *>(ws + lay.pre);
+    const int nt = pre[b + 1] - pre[b];
+    __half *out = static_cast<__half *>(a.out) + static_cast<size_t>(warp) * D + lane * E;
+    if (nt == 0) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[e] = __float2half_rn(0.f);
+        if (lane == 0 && a.lse_out) a.lse_out[warp] = -INFINITY;
+        return;
+    }
+    const long long T = static_cast<long long>(Hk) * pre[B];
+    const long long x0 = static_cast<long long>(Hk) * pre[b] + static_cast<long long>(j) * nt;
+    const long long x1 = x0 + nt - 1;
+    // worker holding unit x: the largest w with w*T/W <= x
+    auto owner = [&](long long x) { return static_cast<int>(((x + 1) * workers + T - 1) / T - 1); };
+    const int wf = owner(x0);
+    const int wl = owner(x1);
+    if (wf == wl) return;  // written whole by one worker
+    const bool wf_starts_here = (static_cast<long long>(wf) * T / workers) == x0;
+    const int np = wl - wf + 1;
+    const float *pm = reinterpret_cast<const float *>(ws + lay.m);
+    const float *pl = reinterpret_cast<const float *>(ws + lay.l);
+    const float *pacc = reinterpret_cast<const float *>(ws + lay.acc);
+    auto piece = [&](int i) {
+        const int wk = wf + i;
+        const int slot = (i == 0 && !wf_starts_here) ? 1 : 0;
+        return (static_cast<size_t>(wk) * 2 + slot) * G + gi;
+    };
+    // pieces with m = -inf (empty workers, skipped blocks) carry no weight
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32) M = fmaxf(M, pm[piece(i)]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M == -INFINITY) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[e] = __float2half_rn(0.f);
+        if (lane == 0 && a.lse_out) a.lse_out[warp] = -INFINITY;
+        return;
+    }
+    float tot = 0.f;
+    for (int i = lane; i < np; i += 32) {
+        const size_t pi = piece(i);
+        const float mi = pm[pi];
+        if (mi != -INFINITY) tot = fmaf(exp2f(mi - M), pl[pi], tot);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int i = 0; i < np; ++i) {
+        const size_t pi = piece(i);
+        const float mi = pm[pi];
+        if (mi == -INFINITY) continue;
+        const float wgt = exp2f(mi - M);
+        const float *src = pacc + pi * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, src[e], acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = __float2half_rn(acc[e] / tot);
+    if (lane == 0 && a.lse_out) a.lse_out[warp] = (M + log2f(tot)) * kLn2b;
+}
+
+template <int D, int G>
+size_t bal_smem(int B) {
+    using C = BalCfg<D, G>;
+    return 1024 + C::PIPE_BYTES + C::QS_BYTES + (2 * static_cast<size_t>(B) + 1) * 4;
+}
+
+template <int D, int G>
+int bal_ctas_per_sm(int B) {
+    static std::mutex mu;
+    static std::map<size_t, int> cache;
+    const size_t smem = bal_smem<D, G>(B);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(smem);
+    if (it != cache.end()) return it->second;
+    auto kern = decode_balanced_kernel<D, G>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bal_smem<D, G>(kMaxSeqsBalanced))) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreadsB, smem) != cudaSuccess)
+        return 0;
+    cache[smem] = n;
+    return n;
+}
+
+template <int D, int G>
+cudaError_t launch_bal_t(const DecodeArgs &a, const BalancedPlan &plan, const CUtensorMap &tk,
+                         const CUtensorMap &tv, cudaStream_t stream) {
+    auto kern = decode_balanced_kernel<D, G>;
+    if (bal_ctas_per_sm<D, G>(a.num_seqs) <= 0) return cudaErrorInvalidConfiguration;
+    cudaError_t e = launch_pdl(kern, dim3(plan.ctas), dim3(kThreadsB),
+                               bal_smem<D, G>(a.num_seqs), stream, a, tk, tv, plan.workers);
+    if (e != cudaSuccess) return e;
+    const long long warps = static_cast<long long>(a.num_seqs) * a.n_q_heads;
+    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+    return launch_pdl(balanced_merge_kernel<D, G>, dim3(blocks), dim3(256), 0, stream, a,
+                      plan.workers);
+}
+
+int sm_count_cached() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess)
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    });
+    return n;
+}
+
+}  // namespace
+
+bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
+                        long long cache_rows) {
+    return num_seqs >= 1 && num_seqs <= kMaxSeqsBalanced && (head_dim == 64 || head_dim == 128) &&
+           (group == 1 || group == 2 || group == 4 || group == 8) && block_size % kMmaTile == 0 &&
+           cache_rows < (1LL << 31);
+}
+
+bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
+                   BalancedPlan *plan) {
+    const int G = n_q_heads / n_kv_heads;
+    int per_sm = 0;
+#define PKV_BAL_OCC(D_, G_) \
+    if (head_dim == D_ && G == G_) per_sm = bal_ctas_per_sm<D_, G_>(num_seqs);
+    PKV_BAL_OCC(128, 1)
+    PKV_BAL_OCC(128, 2)
+    PKV_BAL_OCC(128, 4)
+    PKV_BAL_OCC(128, 8)
+    PKV_BAL_OCC(64, 1)
+    PKV_BAL_OCC(64, 2)
+    PKV_BAL_OCC(64, 4)
+    PKV_BAL_OCC(64, 8)
+#undef PKV_BAL_OCC
+    const int sms = sm_count_cached();
+    if (per_sm <= 0 || sms <= 0) return false;
+    // upper bound on the units; at least 2 tiles per warp on average
+    const long long t_max = static_cast<long long>(n_kv_heads) * num_seqs *
+                            ((static_cast<long long>(max_len) + kMmaTile - 1) / kMmaTile);
+    long long ctas = static_cast<long long>(sms) * per_sm;
+    const long long need = (t_max + 2 * kW - 1) / (2 * kW);
+    if (need < ctas) ctas = need;
+    if (ctas < 1) ctas = 1;
+    plan->ctas = static_cast<int>(ctas);
+    plan->workers = plan->ctas * kW;
+    plan->ws_bytes = bal_layout(num_seqs, plan->workers, G, head_dim).total;
+    return true;
+}
+
+cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
+                                   cudaStream_t stream) {
+    const long long rows = a.num_blocks * a.n_kv_heads * static_cast<long long>(a.block_size);
+    CUtensorMap tk, tv;
+    if (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
+        !make_cache_map(&tv, a.v_cache, rows, a.head_dim))
+        return cudaErrorNotSupported;
+    const int g = a.n_q_heads / a.n_kv_heads;
+#define PKV_BAL_CASE(D_, G_) \
+    if (a.head_dim == D_ && g == G_) return launch_bal_t<D_, G_>(a, plan, tk, tv, stream);
+    PKV_BAL_CASE(128, 1)
+    PKV_BAL_CASE(128, 2)
+    PKV_BAL_CASE(128, 4)
+    PKV_BAL_CASE(128, 8)
+    PKV_BAL_CASE(64, 1)
+    PKV_BAL_CASE(64, 2)
+    PKV_BAL_CASE(64, 4)
+    PKV_BAL_CASE(64, 8)
+#undef PKV_BAL_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

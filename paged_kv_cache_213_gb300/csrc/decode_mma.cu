@@ -28,26 +28,22 @@
 
 #include "pagedkv.h"
 #include "pkv_internal.h"
+#include "mma_tile.cuh"
 #include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kTile = 16;
+constexpr int kTile = kMmaTile;
 constexpr int kWarps = 4;
 constexpr int kStages = 2;  // per warp
 constexpr int kThreadsMma = kWarps * 32;
 constexpr float kLn2f = 0.69314718055994531f;
 
 template <int D>
-struct MmaCfg {
-    static constexpr int BOXES = D / 64;            // 64-column TMA boxes per tile
-    static constexpr int BOX_BYTES = kTile * 128;   // 16 rows x 128 B
-    static constexpr int TILE_BYTES = BOXES * BOX_BYTES;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
+struct GridCfg : MmaCfg<D> {
+    static constexpr int STAGE_BYTES = 2 * MmaCfg<D>::TILE_BYTES;  // K then V
     static constexpr int PIPE_BYTES = kWarps * kStages * STAGE_BYTES;
-    static constexpr int NP = D / 32;               // 16-byte pieces per row per thread
-    static constexpr int NB_D = D / 8;              // 8-column output blocks
 };
 
 __device__ __forceinline__ int checked_len_mma(const DecodeArgs &a, int b, bool flag) {
@@ -66,7 +62,7 @@ __global__ void __launch_bounds__(kThreadsMma)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a,
                       const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
-    using C = MmaCfg<D>;
+    using C = GridCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kWarps][kStages];
     // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1 KiB
@@ -119,21 +115,10 @@ __global__ void __launch_bounds__(kThreadsMma)
     // MMA k-step 2p+sub uses words 2*sub (k = 2tq, 2tq+1) and 2*sub+1
     // (k = 2tq+8, 2tq+9) of piece p, for Q and K alike.
     uint32_t qa[C::NP][4];
-#pragma unroll
-    for (int p = 0; p < C::NP; ++p) {
-        const int col = (p >> 1) * 64 + (2 * tq + (p & 1)) * 8;
-        if (g < G) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(
-                static_cast<const __half *>(a.q) +
-                (static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + g) * D + col);
-            qa[p][0] = v.x;
-            qa[p][1] = v.y;
-            qa[p][2] = v.z;
-            qa[p][3] = v.w;
-        } else {
-            qa[p][0] = qa[p][1] = qa[p][2] = qa[p][3] = 0u;
-        }
-    }
+    load_q_frag<D>(qa,
+                   static_cast<const __half *>(a.q) +
+                       (static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + (g < G ? g : 0)) * D,
+                   g < G, tq);
     __syncthreads();
 
     unsigned char *my_stages = smem + warp * kStages * C::STAGE_BYTES;
@@ -183,82 +168,7 @@ __global__ void __launch_bounds__(kThreadsMma)
         const int tok0 = t_begin + i * kTile;
         int n_valid = min(kTile, t_end - tok0);
         if (s_blk[tok0 / bs - lb0] < 0) n_valid = 0;
-        if (n_valid < kTile) {
-            // rows past the sequence (or of a skipped block) must not reach P.V
-            const int per_row = C::BOXES * 8;
-            for (int idx = lane; idx < (kTile - n_valid) * per_row; idx += 32) {
-                const int r = n_valid + idx / per_row;
-                const int rem = idx % per_row;
-                *reinterpret_cast<uint4 *>(vs + (rem >> 3) * C::BOX_BYTES + r * 128 +
-                                           (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        // S = Q K^T for tokens 0-7 (nb = 0) and 8-15 (nb = 1) of the tile
-        float sacc[2][4];
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
-            sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
-            const int t = nb * 8 + g;
-#pragma unroll
-            for (int p = 0; p < C::NP; ++p) {
-                const int unit = 2 * tq + (p & 1);
-                const uint4 kw = *reinterpret_cast<const uint4 *>(
-                    ks + (p >> 1) * C::BOX_BYTES + t * 128 + ((unit ^ g) << 4));
-                const uint32_t a0[4] = {qa[p][0], 0u, qa[p][1], 0u};
-                mma_16816(sacc[nb], a0, kw.x, kw.y);
-                const uint32_t a1[4] = {qa[p][2], 0u, qa[p][3], 0u};
-                mma_16816(sacc[nb], a1, kw.z, kw.w);
-            }
-        }
-        // online softmax for head g over this tile's tokens 2tq, 2tq+1, 8+2tq, 9+2tq
-        float s[2][2];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tt = nb * 8 + 2 * tq + e;
-                s[nb][e] = tt < n_valid ? sacc[nb][e] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[nb][e]);
-            }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-        float pv[2][2];
-        float psum = 0.f;
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                pv[nb][e] = (s[nb][e] == -INFINITY) ? 0.f : exp2f(s[nb][e] - m_new);
-                psum += pv[nb][e];
-            }
-        l_run = l_run * corr + psum;
-        m_run = m_new;
-#pragma unroll
-        for (int n = 0; n < C::NB_D; ++n) {
-            o[n][0] *= corr;
-            o[n][1] *= corr;
-        }
-        const uint32_t pa[4] = {pack_half2(pv[0][0], pv[0][1]), 0u,
-                                pack_half2(pv[1][0], pv[1][1]), 0u};
-        // O += P V: V fragments by transposing 8x8 loads, two 8-column blocks per load
-        const int lm = lane >> 3;
-        const int ri = lane & 7;
-        const int vt = ((lm & 1) << 3) + ri;
-#pragma unroll
-        for (int qd = 0; qd < C::NB_D / 2; ++qd) {
-            const int u = 2 * qd + (lm >> 1);
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(r0, r1, r2, r3,
-                          vs + (u >> 3) * C::BOX_BYTES + vt * 128 + (((u & 7) ^ ri) << 4));
-            mma_16816(o[2 * qd], pa, r0, r1);
-            mma_16816(o[2 * qd + 1], pa, r2, r3);
-        }
+        mma_tile<D>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
         __syncwarp();
         if (k + kStages < my_tiles) {
             if (lane == 0) issue(i + kStages * kWarps, slot);
@@ -337,6 +247,27 @@ __global__ void __launch_bounds__(kThreadsMma)
     }
 }
 
+template <int D, int G>
+cudaError_t launch_mma_t(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                         cudaStream_t stream) {
+    using C = GridCfg<D>;
+    const int ids = (a.partition_tokens / a.block_size + 3) / 4 * 4;
+    const size_t smem = 1024 + C::PIPE_BYTES + static_cast<size_t>(ids) * 4;
+    auto kern = decode_mma_kernel<D, G>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        1024 + C::PIPE_BYTES + 2048 * 4);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid(a.num_seqs, a.n_kv_heads, a.max_parts);
+    kern<<<grid, kThreadsMma, smem, stream>>>(a, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 // cuTensorMapEncodeTiled from the driver, looked up once.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
@@ -367,27 +298,6 @@ bool make_cache_map(CUtensorMap *m, const void *base, long long rows, int D) {
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-template <int D, int G>
-cudaError_t launch_mma_t(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                         cudaStream_t stream) {
-    using C = MmaCfg<D>;
-    const int ids = (a.partition_tokens / a.block_size + 3) / 4 * 4;
-    const size_t smem = 1024 + C::PIPE_BYTES + static_cast<size_t>(ids) * 4;
-    auto kern = decode_mma_kernel<D, G>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        1024 + C::PIPE_BYTES + 2048 * 4);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid(a.num_seqs, a.n_kv_heads, a.max_parts);
-    kern<<<grid, kThreadsMma, smem, stream>>>(a, tk, tv);
-    return cudaGetLastError();
-}
-
-}  // namespace
 
 bool decode_mma_supported(const DecodeArgs &a) {
     const int g = a.n_q_heads / a.n_kv_heads;

@@ -1,0 +1,145 @@
+// mma_tile.cuh -- the per-tile math of the tensor-core decode kernels: one
+// warp, one 16-token K/V tile (TMA-loaded with 128-byte swizzle), the GQA
+// query group as the M dimension of mma.m16n8k16.
+//
+//   S = Q K^T       M = query heads (padded to 16), N = 8 tokens, K = head_dim
+//   online softmax  fp32, exp2 domain, running max / sum per head
+//   O += P V        M = heads, N = 8 head_dim columns, K = 16 tokens
+//
+// Fragment ownership: lane = 4*g + tq.  g is the query head (row of A / C),
+// tq picks columns.  For S = Q K^T the MMA k index is mapped to head_dim so
+// that each thread reads whole 16-byte pieces: piece p (0 .. D/32-1) of a row
+// is the 16 bytes at column 64*(p/2) + 8*(2*tq + p%2); MMA k-step 2p+sub takes
+// its words 2*sub (k = 2tq, 2tq+1) and 2*sub+1 (k = 2tq+8, 2tq+9).  Q and K use
+// the same map, so the dot products are unchanged.  The C fragment of S
+// (tokens 2tq, 2tq+1 of each 8-token block) is exactly the A fragment of P.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+
+constexpr int kMmaTile = 16;  // tokens per tile
+
+template <int D>
+struct MmaCfg {
+    static constexpr int BOXES = D / 64;           // 64-column TMA boxes per tile
+    static constexpr int BOX_BYTES = kMmaTile * 128;  // 16 rows x 128 B
+    static constexpr int TILE_BYTES = BOXES * BOX_BYTES;
+    static constexpr int NP = D / 32;              // 16-byte pieces per row per thread
+    static constexpr int NB_D = D / 8;             // 8-column output blocks
+};
+
+// Byte offset of 16-byte unit `unit` (0-7) of row `row` in a 128B-swizzled box.
+__device__ __forceinline__ int swz(int row, int unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
+
+// Q fragments of head g from a row-major [.., D] fp16 row (global or shared).
+template <int D>
+__device__ __forceinline__ void load_q_frag(uint32_t (&qa)[MmaCfg<D>::NP][4], const __half *row,
+                                            bool present, int tq) {
+#pragma unroll
+    for (int p = 0; p < MmaCfg<D>::NP; ++p) {
+        const int col = (p >> 1) * 64 + (2 * tq + (p & 1)) * 8;
+        if (present) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + col);
+            qa[p][0] = v.x;
+            qa[p][1] = v.y;
+            qa[p][2] = v.z;
+            qa[p][3] = v.w;
+        } else {
+            qa[p][0] = qa[p][1] = qa[p][2] = qa[p][3] = 0u;
+        }
+    }
+}
+
+// One tile: rows [0, n_valid) of the K tile `ks` and V tile `vs` take part;
+// the V rows past n_valid are zeroed first (they may hold another sequence's
+// data or NaN and must not reach P.V).  Updates the running state of head g.
+template <int D>
+__device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char *vs, int n_valid,
+                                         const uint32_t (&qa)[MmaCfg<D>::NP][4],
+                                         float scale_log2, float (&o)[MmaCfg<D>::NB_D][4],
+                                         float &m_run, float &l_run, int lane) {
+    using C = MmaCfg<D>;
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    if (n_valid < kMmaTile) {
+        const int per_row = C::BOXES * 8;
+        for (int idx = lane; idx < (kMmaTile - n_valid) * per_row; idx += 32) {
+            const int r = n_valid + idx / per_row;
+            const int rem = idx % per_row;
+            *reinterpret_cast<uint4 *>(vs + (rem >> 3) * C::BOX_BYTES + r * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // before a later TMA write of these bytes
+        __syncwarp();
+    }
+
+    // S = Q K^T for tokens 0-7 (nb = 0) and 8-15 (nb = 1)
+    float sacc[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+        sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
+        const int t = nb * 8 + g;
+#pragma unroll
+        for (int p = 0; p < C::NP; ++p) {
+            const uint4 kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
+                                                              swz(t, 2 * tq + (p & 1)));
+            const uint32_t a0[4] = {qa[p][0], 0u, qa[p][1], 0u};
+            mma_16816(sacc[nb], a0, kw.x, kw.y);
+            const uint32_t a1[4] = {qa[p][2], 0u, qa[p][3], 0u};
+            mma_16816(sacc[nb], a1, kw.z, kw.w);
+        }
+    }
+    // online softmax of head g over tokens 2tq, 2tq+1, 8+2tq, 9+2tq
+    float s[2][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int tt = nb * 8 + 2 * tq + e;
+            s[nb][e] = tt < n_valid ? sacc[nb][e] * scale_log2 : -INFINITY;
+            mx = fmaxf(mx, s[nb][e]);
+        }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+    float pv[2][2];
+    float psum = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            pv[nb][e] = (s[nb][e] == -INFINITY) ? 0.f : exp2f(s[nb][e] - m_new);
+            psum += pv[nb][e];
+        }
+    l_run = l_run * corr + psum;
+    m_run = m_new;
+#pragma unroll
+    for (int n = 0; n < C::NB_D; ++n) {
+        o[n][0] *= corr;
+        o[n][1] *= corr;
+    }
+    const uint32_t pa[4] = {pack_half2(pv[0][0], pv[0][1]), 0u, pack_half2(pv[1][0], pv[1][1]),
+                            0u};
+    // O += P V: V fragments by transposed 8x8 loads, two 8-column blocks per load
+    const int lm = lane >> 3;
+    const int ri = lane & 7;
+    const int vt = ((lm & 1) << 3) + ri;
+#pragma unroll
+    for (int qd = 0; qd < C::NB_D / 2; ++qd) {
+        const int u = 2 * qd + (lm >> 1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
+        mma_16816(o[2 * qd], pa, r0, r1);
+        mma_16816(o[2 * qd + 1], pa, r2, r3);
+    }
+}
+
+}  // namespace pkv

@@ -4,9 +4,31 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace pkv {
+
+// Launch with the programmatic stream-serialization attribute, so that the
+// kernel's CTAs may be scheduled while the previous kernel in the stream
+// drains; the kernel must call grid_dependency_wait() before touching memory
+// that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct AppendArgs {
     const void *k_new;
@@ -57,8 +79,27 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
 // Returns cudaErrorInvalidValue for a (head_dim, group) pair with no kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 bool decode_supported(int head_dim, int group);
+// PKV_DECODE_KERNEL: 0 unset (automatic), 1 "simt", 2 "mma" (the grid kernels).
+int kernel_override();
 // Tensor-core kernel (decode_mma.cu): partition pass only, no merge.
 bool decode_mma_supported(const DecodeArgs &a);
 cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t stream);
+// 2-D TMA map [rows][D] fp16 of a cache, 16x64 boxes, 128-byte swizzle.
+bool make_cache_map(CUtensorMap *m, const void *base, long long rows, int D);
+
+// Balanced (work-split per warp) tensor-core kernel (decode_balanced.cu).
+struct BalancedPlan {
+    int ctas;        // grid size
+    int workers;     // warps doing work = 4 * ctas
+    size_t ws_bytes; // workspace bytes
+};
+bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
+                        long long cache_rows);
+// Grid and workspace for the balanced kernel (host query of the SM count
+// and occupancy); false if the device query fails.
+bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
+                   BalancedPlan *plan);
+cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
+                                   cudaStream_t stream);
 
 }  // namespace pkv

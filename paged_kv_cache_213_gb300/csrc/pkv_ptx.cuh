@@ -160,3 +160,19 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 }  // namespace pkv
+
+namespace pkv {
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the previous kernel in the
+// stream finishes; grid_dependency_wait() blocks until that kernel has
+// completed and its writes are visible (a no-op without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next programmatically dependent kernel in the stream launch now.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace pkv

@@ -82,7 +82,8 @@ def _randn16(rng, shape):
 
 def make_batch(name, lens, n_q_heads, n_kv_heads, head_dim, block_size, rng, *,
                scale=None, pool_blocks=None, pool_extra=0.10, shared=None, append=True,
-               poison=True, max_blocks_per_seq=None, append_padding=0):
+               poison=True, max_blocks_per_seq=None, append_padding=0,
+               physical_order="random"):
     """Build one batch.
 
     lens: attention length per sequence (the appended token included).
@@ -93,6 +94,8 @@ def make_batch(name, lens, n_q_heads, n_kv_heads, head_dim, block_size, rng, *,
     append: also build k_new / v_new / slot_mapping for one new token per
       sequence, written at position L-1 (that cache row holds poison or noise).
     append_padding: number of extra padding tokens (slot -1) in the append.
+    physical_order: "random" (a random permutation of the pool) or "identity"
+      (blocks laid out in logical order, for comparisons of access patterns).
     """
     lens = np.asarray(lens, dtype=np.int64)
     B = len(lens)
@@ -127,7 +130,10 @@ def make_batch(name, lens, n_q_heads, n_kv_heads, head_dim, block_size, rng, *,
     NB = pool_blocks if pool_blocks is not None else used + int(math.ceil(pool_extra * used))
     if NB < used:
         raise ValueError("pool too small")
-    perm = rng.permutation(NB).astype(np.int32)
+    if physical_order == "identity":
+        perm = np.arange(NB, dtype=np.int32)
+    else:
+        perm = rng.permutation(NB).astype(np.int32)
     phys_of = perm[:used]           # k-th unique block -> physical id
 
     bt = np.empty((B, MB), dtype=np.int32)

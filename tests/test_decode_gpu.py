@@ -251,3 +251,32 @@ def test_side_stream_and_reuse():
     assert np.array_equal(outs[0].cpu().numpy().view(np.uint16),
                           outs[2].cpu().numpy().view(np.uint16))
     assert math.isfinite(float(compare(outs[1].cpu().numpy(), ref["out"])[0]))
+
+
+@pytest.mark.parametrize("lens_kind", ["many_short", "single_unit", "mixed_empty", "over_2048"])
+def test_balanced_split_shapes(lens_kind):
+    """The default (balanced) split with segments much shorter than a warp's
+    range, a single unit of work, empty sequences mixed in, and a batch too
+    large for the balanced kernel (falls back to the partition grid)."""
+    rng = np.random.default_rng({"many_short": 1, "single_unit": 2, "mixed_empty": 3,
+                                 "over_2048": 4}[lens_kind])
+    if lens_kind == "many_short":
+        lens = rng.integers(1, 41, size=700)
+        H, Hk, d = 8, 2, 128
+    elif lens_kind == "single_unit":
+        lens = [1]
+        H, Hk, d = 4, 1, 64
+    elif lens_kind == "mixed_empty":
+        lens = [0, 3000, 0, 0, 17, 1, 0, 900, 0]
+        H, Hk, d = 32, 8, 128
+    else:
+        lens = rng.integers(1, 70, size=2100)
+        H, Hk, d = 4, 1, 64
+    batch = wl.make_batch(lens_kind, lens, H, Hk, d, 16, rng, append=False, poison=True)
+    g = gpu_step(batch)
+    assert g["err"] == 0
+    ref = oracle_step(batch)
+    assert_close(g["out"], ref["out"], what=lens_kind)
+    fin = np.isfinite(ref["lse"])
+    assert np.max(np.abs(g["lse"][fin] - ref["lse"][fin])) <= 1e-4
+    assert np.all(np.isneginf(g["lse"][~fin]))
