@@ -295,7 +295,7 @@ def run_ours(args):
     mcl = batch.max_context_len
     P, ws_bytes = pkv.decode_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
                                   args.partition)
-    work = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    work = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 else 0)
 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size

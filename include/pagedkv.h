@@ -152,7 +152,10 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
  *  workspace      device scratch of at least the planned bytes (256-byte
  *                 aligned), may be NULL when the plan needs 0 bytes; the
  *                 caller owns it; calls that overlap in time need separate
- *                 workspaces
+ *                 workspaces.  It must be zero-filled before its first use:
+ *                 the balanced split keeps per-segment arrival counters at
+ *                 its start, and every call leaves them zero again (after a
+ *                 call that flagged PKV_ERRBIT_TIMEOUT, zero it once more)
  *  lse_out        device fp32 [num_seqs][n_q_heads] natural-log sum of
  *                 exp(logits), may be NULL
  *  err_word       device int32, may be NULL (see the header comment)

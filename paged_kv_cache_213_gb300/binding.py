@@ -189,7 +189,8 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         _need(err_word, "err_word", torch.int32, dev)
     if ws_bytes > 0:
         if workspace is None:
-            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            # zero-filled: the balanced split keeps arrival counters in it
+            workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         else:
             _need(workspace, "workspace", torch.uint8, dev)
     with torch.cuda.device(dev):

@@ -2,15 +2,19 @@
 // over warps (the default tensor-core path).
 //
 // The work of one call is the list of (sequence b, KV head j, 16-token tile t)
-// units, ordered b, then j, then t: T units in all.  Each of the W warps of
-// the grid (W = 4 x number of CTAs, sized to fill every SM once) takes the
-// contiguous range [w*T/W, (w+1)*T/W), so every warp moves the same number of
-// K/V bytes (+-1 tile) whatever the mix of context lengths.  A warp streams
-// its range through its own 2-stage ring of TMA-loaded tiles, carrying the
-// online-softmax state of the current (b, j) "segment".  When a segment ends
-// inside the range the warp writes the final output; a segment cut by a range
-// boundary leaves a partial result (m, l, acc) in one of the warp's two
-// workspace slots, and a second kernel merges those by log-sum-exp.
+// units, ordered b, then j, then t: T units in all.  The W warps of the grid
+// (W = 4 x number of CTAs, sized to fill every SM once) take consecutive
+// ranges of U = ceil(T / W) units each, so every warp moves the same number of
+// K/V bytes whatever the mix of context lengths.  A warp streams its range
+// through its own ring of TMA-loaded tiles, carrying the online-softmax state
+// of the current (b, j) "segment".  A segment that ends inside the range is
+// written out directly.  A segment cut by range boundaries leaves one partial
+// result (m, l, acc) per warp; each such warp then bumps the segment's arrival
+// counter, and the warp that arrives last merges all partials by log-sum-exp,
+// writes the output and resets the counter to zero -- there is no second
+// kernel.  The counters live at the start of the caller's workspace, which
+// must therefore be zero-filled before its first use; every call leaves them
+// zero again.
 //
 // Method: "Distributed LLM Inference Serving Platform", sections 2-3 (block
 // table gather) and 5.1 (attention over every block of a sequence's table),
@@ -23,7 +27,6 @@
 #include <cmath>
 #include <map>
 #include <mutex>
-#include <tuple>
 
 #include "mma_tile.cuh"
 #include "pagedkv.h"
@@ -40,6 +43,7 @@ constexpr int kW = 4;  // warps per CTA, each an independent worker
 constexpr int kS = PKV_BAL_STAGES;  // ring stages per warp
 constexpr int kThreadsB = kW * 32;
 constexpr int kMaxSeqsBalanced = 2048;
+constexpr int kMaxWorkers = 16384;  // size of the counter region
 constexpr float kLn2b = 0.69314718055994531f;
 
 template <int D, int G>
@@ -50,20 +54,16 @@ struct BalCfg : MmaCfg<D> {
     static constexpr int QS_BYTES = kW * kS * Q_BYTES;
 };
 
-// Workspace: int pre[B+1] (tile prefix over sequences), then per worker two
-// piece slots: acc [W][2][G][D], m [W][2][G], l [W][2][G] (fp32).
-struct BalLayout {
-    size_t pre, acc, m, l, total;
-};
-__host__ __device__ inline BalLayout bal_layout(int B, int workers, int G, int D) {
-    BalLayout L{};
-    const size_t slots = static_cast<size_t>(workers) * 2 * G;
-    L.pre = 0;
-    L.acc = ((static_cast<size_t>(B) + 1) * 4 + 255) / 256 * 256;
-    L.m = L.acc + (slots * D * 4 + 255) / 256 * 256;
-    L.l = L.m + (slots * 4 + 255) / 256 * 256;
-    L.total = L.l + (slots * 4 + 255) / 256 * 256;
-    return L;
+// Workspace: int counters[kMaxWorkers] at offset 0 (whatever the plan, so
+// that a workspace reused by another plan still starts zeroed), then one
+// record per (worker, slot 0/1): acc [G][D], m [G], l [G] (fp32), padded to a
+// multiple of 16 bytes so that a record is one bulk copy.
+__host__ __device__ constexpr size_t rec_bytes(int G, int D) {
+    return (static_cast<size_t>(G) * (D + 2) * 4 + 15) / 16 * 16;
+}
+constexpr size_t kRecBase = static_cast<size_t>(kMaxWorkers) * 4;
+__host__ __device__ inline size_t bal_ws_bytes(int workers, int G, int D) {
+    return kRecBase + static_cast<size_t>(workers) * 2 * rec_bytes(G, D);
 }
 
 __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b, bool flag) {
@@ -83,13 +83,13 @@ struct Cursor {
     int b, j, t;
 };
 
-__device__ __forceinline__ Cursor locate(long long x, const int *pre, int B, int Hk) {
+__device__ __forceinline__ Cursor locate(int x, const int *pre, int B, int Hk) {
     int lo = 0, hi = B - 1;  // largest b with Hk * pre[b] <= x
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<long long>(Hk) * pre[mid] <= x) lo = mid; else hi = mid - 1;
+        if (Hk * pre[mid] <= x) lo = mid; else hi = mid - 1;
     }
-    const int r = static_cast<int>(x - static_cast<long long>(Hk) * pre[lo]);  // < Hk * nt
+    const int r = x - Hk * pre[lo];
     const int nt = pre[lo + 1] - pre[lo];
     return Cursor{lo, r / nt, r % nt};
 }
@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kThreadsB)
     using C = BalCfg<D, G>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kW][kS];
+    __shared__ uint64_t merge_bar[kW];
     __shared__ int s_ok[kW][kS];
     __shared__ int s_scan[kW];
     const uint32_t raw_s = smem_addr(smem_raw);
@@ -129,10 +130,9 @@ __global__ void __launch_bounds__(kThreadsB)
     const int H = a.n_q_heads;
     const int Hk = a.n_kv_heads;
     const int bs = a.block_size;
-    const BalLayout lay = bal_layout(B, workers, G, D);
     char *ws = reinterpret_cast<char *>(a.ws_acc);
-    grid_dependency_wait();    // the previous kernel (e.g. the append) is done
-    allow_dependent_launch();  // the merge kernel may get scheduled meanwhile
+    int *counters = reinterpret_cast<int *>(ws);
+    grid_dependency_wait();  // the previous kernel in the stream (e.g. the append) is done
 
     // --- tile prefix over sequences: contiguous chunk per thread, then a scan
     const int chunk = (B + kThreadsB - 1) / kThreadsB;
@@ -154,8 +154,10 @@ __global__ void __launch_bounds__(kThreadsB)
     if (tid == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
-        for (int w = 0; w < kW; ++w)
+        for (int w = 0; w < kW; ++w) {
             for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
+            mbar_init(&merge_bar[w], 1);
+        }
         fence_barrier_init();
     }
     __syncthreads();
@@ -168,20 +170,23 @@ __global__ void __launch_bounds__(kThreadsB)
     }
     if (tid == kThreadsB - 1) s_pre[B] = base + incl;
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int b = tid; b <= B; b += kThreadsB) reinterpret_cast<int *>(ws + lay.pre)[b] = s_pre[b];
 
-    // --- this warp's range of units
-    const int w = blockIdx.x * kW + warp;
-    const long long T = static_cast<long long>(Hk) * s_pre[B];
-    const long long w0 = w * T / workers;
-    const long long w1 = (w + 1) * T / workers;
-    const int n = static_cast<int>(w1 - w0);
-    if (n <= 0) {  // more warps than units: mark the slot the merge may visit as empty
-        if (g < G && tq == 0)
-            reinterpret_cast<float *>(ws + lay.m)[(static_cast<size_t>(w) * 2) * G + g] = -INFINITY;
-        return;  // no further CTA-wide barriers below
+    // empty sequences: out = 0, lse = -inf (sequences spread over the CTAs)
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        if (s_len[b] != 0) continue;
+        __half *ob = static_cast<__half *>(a.out) + static_cast<size_t>(b) * H * D;
+        for (int i = tid; i < H * D; i += kThreadsB) ob[i] = __float2half_rn(0.f);
+        if (a.lse_out)
+            for (int h = tid; h < H; h += kThreadsB) a.lse_out[static_cast<size_t>(b) * H + h] = -INFINITY;
     }
+
+    // --- this warp's range of units: [w * U, (w + 1) * U) clipped to T
+    const int w = blockIdx.x * kW + warp;
+    const int T = Hk * s_pre[B];
+    const int U = (T + workers - 1) / workers;
+    const int w0 = static_cast<int>(min(static_cast<long long>(T), static_cast<long long>(w) * U));
+    const int n = min(T, w0 + U) - w0;
+    if (n <= 0) return;  // no CTA-wide barriers below
 
     unsigned char *my_pipe = smem + warp * kS * C::SLOT_BYTES;
     unsigned char *my_q = qslots + warp * kS * C::Q_BYTES;
@@ -192,8 +197,8 @@ __global__ void __launch_bounds__(kThreadsB)
     // Block ids of the range, 32 tiles at a time: lane i holds the id of tile
     // 32c + i, for the chunk c being issued (ids_cur) and the next (ids_next),
     // so no table load sits on the issue path.
-    auto load_ids = [&](int chunk) -> int {
-        const int kk = chunk * 32 + lane;
+    auto load_ids = [&](int chunk_no) -> int {
+        const int kk = chunk_no * 32 + lane;
         if (kk >= n) return -1;
         const Cursor c = locate(w0 + kk, s_pre, B, Hk);
         return a.block_tables[static_cast<size_t>(c.b) * a.max_blocks_per_seq +
@@ -249,35 +254,115 @@ __global__ void __launch_bounds__(kThreadsB)
     float m_run = -INFINITY, l_run = 0.f;
     int cur_seg = -1, pb = 0, pj = 0, piece_t0 = 0, last_t = 0, piece_no = 0;
 
+    constexpr size_t REC = rec_bytes(G, D);
+    auto rec = [&](int wk, int slot) { return ws + kRecBase + (static_cast<size_t>(wk) * 2 + slot) * REC; };
+    const int gg = g < G ? g : 0;
+
+    // Output row of head gg of segment (b, j): o / l in fp16, lse.
+    auto write_out = [&](int b, int j, float fm, float fl) {
+        if (g >= G) return;
+        const size_t bh = static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + g;
+        const float inv = fl > 0.f ? 1.f / fl : 0.f;
+        __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
+#pragma unroll
+        for (int nb = 0; nb < C::NB_D; ++nb)
+            dst[nb * 4 + tq] = __floats2half2_rn(o[nb][0] * inv, o[nb][1] * inv);
+        if (tq == 0 && a.lse_out) a.lse_out[bh] = fl > 0.f ? (fm + log2f(fl)) * kLn2b : -INFINITY;
+    };
+
+    // Cut segments this warp arrived last on, merged once its ring is idle.
+    int pend_n = 0, pend_b[2], pend_j[2], pend_x0[2], pend_nt[2];
+
     // Writes the finished piece [piece_t0, last_t] of segment (pb, pj).
     auto flush = [&]() {
         float lt = l_run;
         lt += __shfl_xor_sync(0xffffffffu, lt, 1);
         lt += __shfl_xor_sync(0xffffffffu, lt, 2);
         const int nt = s_pre[pb + 1] - s_pre[pb];
-        const bool complete = piece_t0 == 0 && last_t == nt - 1;
+        if (piece_t0 == 0 && last_t == nt - 1) {  // the whole segment: write it out
+            write_out(pb, pj, m_run, lt);
+            ++piece_no;
+            return;
+        }
+        // a cut segment: publish this piece as a record, then count the arrivals
+        char *r = rec(w, piece_no == 0 ? 0 : 1);
         if (g < G) {
-            const size_t bh = static_cast<size_t>(pb) * H + static_cast<size_t>(pj) * G + g;
-            if (complete) {
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
-                __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
+            float2 *acc = reinterpret_cast<float2 *>(r) + static_cast<size_t>(g) * (D / 2);
 #pragma unroll
-                for (int nb = 0; nb < C::NB_D; ++nb)
-                    dst[nb * 4 + tq] = __floats2half2_rn(o[nb][0] * inv, o[nb][1] * inv);
-                if (tq == 0 && a.lse_out)
-                    a.lse_out[bh] = lt > 0.f ? (m_run + log2f(lt)) * kLn2b : -INFINITY;
-            } else {
-                const size_t pi = (static_cast<size_t>(w) * 2 + (piece_no == 0 ? 0 : 1)) * G + g;
-                float2 *acc = reinterpret_cast<float2 *>(ws + lay.acc) + pi * (D / 2);
-#pragma unroll
-                for (int nb = 0; nb < C::NB_D; ++nb) acc[nb * 4 + tq] = make_float2(o[nb][0], o[nb][1]);
-                if (tq == 0) {
-                    reinterpret_cast<float *>(ws + lay.m)[pi] = m_run;
-                    reinterpret_cast<float *>(ws + lay.l)[pi] = lt;
-                }
+            for (int nb = 0; nb < C::NB_D; ++nb) acc[nb * 4 + tq] = make_float2(o[nb][0], o[nb][1]);
+            if (tq == 0) {
+                reinterpret_cast<float *>(r)[G * D + g] = m_run;
+                reinterpret_cast<float *>(r)[G * D + G + g] = lt;
             }
         }
+        __syncwarp();  // the record's stores, all lanes, before lane 0's release
+        const int x0 = Hk * s_pre[pb] + pj * nt;  // the segment's units [x0, x0 + nt)
+        const int wf = x0 / U;
+        const int wl = (x0 + nt - 1) / U;
+        int old = 0;
+        if (lane == 0) old = atomic_add_acq_rel_gpu(&counters[wf], 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
         ++piece_no;
+        if (old == wl - wf) {  // arrived last: merge later, when the ring is idle
+            pend_b[pend_n] = pb;
+            pend_j[pend_n] = pj;
+            pend_x0[pend_n] = x0;
+            pend_nt[pend_n] = nt;
+            ++pend_n;
+        }
+    };
+
+    // Merge all records of a cut segment: bulk-copy them into this warp's
+    // (idle) ring, combine by log-sum-exp, write the output, reset the counter.
+    uint32_t merge_phase = 0;
+    auto merge = [&](int b, int j, int x0, int nt) -> bool {
+        // the acquiring atomic (lane 0) made the other warps' records visible;
+        // order them before the bulk copies (async proxy) that read them
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const int wf = x0 / U;
+        const int wl = (x0 + nt - 1) / U;
+        const bool wf_starts_here = wf * U == x0;
+        constexpr int cap = static_cast<int>((kS * C::SLOT_BYTES) / REC);
+        float M = -INFINITY, Lsum = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < C::NB_D; ++nb) o[nb][0] = o[nb][1] = 0.f;
+        for (int first = wf; first <= wl; first += cap) {
+            const int cnt = min(cap, wl - first + 1);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&merge_bar[warp], static_cast<uint32_t>(cnt * REC));
+                for (int i = 0; i < cnt; ++i) {
+                    const int wk = first + i;
+                    const int slot = (wk == wf && !wf_starts_here) ? 1 : 0;
+                    bulk_copy_g2s(my_pipe + i * REC, rec(wk, slot), static_cast<uint32_t>(REC),
+                                  &merge_bar[warp]);
+                }
+            }
+            const bool ok = mbar_wait_bounded(&merge_bar[warp], merge_phase & 1);
+            ++merge_phase;
+            if (__any_sync(0xffffffffu, !ok)) return false;
+            for (int i = 0; i < cnt; ++i) {
+                const float *rf = reinterpret_cast<const float *>(my_pipe + i * REC);
+                const float mi = rf[G * D + gg];
+                if (mi == -INFINITY) continue;  // a piece of skipped blocks only
+                const float li = rf[G * D + G + gg];
+                const float Mn = fmaxf(M, mi);
+                const float so = exp2f(M - Mn);  // 0 while M = -inf
+                const float sn = exp2f(mi - Mn);
+                Lsum = Lsum * so + li * sn;
+                const float2 *acc = reinterpret_cast<const float2 *>(rf) + static_cast<size_t>(gg) * (D / 2);
+#pragma unroll
+                for (int nb = 0; nb < C::NB_D; ++nb) {
+                    const float2 v = acc[nb * 4 + tq];
+                    o[nb][0] = o[nb][0] * so + v.x * sn;
+                    o[nb][1] = o[nb][1] * so + v.y * sn;
+                }
+                M = Mn;
+            }
+            __syncwarp();  // before the next round overwrites the staged records
+        }
+        if (lane == 0) store_relaxed_gpu(&counters[wf], 0);  // ready for the next call
+        write_out(b, j, M, Lsum);
+        return true;
     };
 
     int k = 0;
@@ -325,88 +410,13 @@ __global__ void __launch_bounds__(kThreadsB)
         return;
     }
     if (cur_seg >= 0) flush();
-}
-
-// One warp per (sequence, query head): segments cut over several workers are
-// merged by log-sum-exp; empty sequences get out = 0, lse = -inf.
-template <int D, int G>
-__global__ void __launch_bounds__(256)
-    balanced_merge_kernel(const __grid_constant__ DecodeArgs a, const int workers) {
-    constexpr int E = D / 32;
-    const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) / 32);
-    const int lane = threadIdx.x % 32;
-    const int B = a.num_seqs;
-    const int H = a.n_q_heads;
-    const int Hk = a.n_kv_heads;
-    grid_dependency_wait();  // the decode kernel's partial results are visible
-    if (warp >= B * H) return;
-    const int b = warp / H;
-    const int h = warp % H;
-    const int j = h / G;
-    const int gi = h % G;
-    const BalLayout lay = bal_layout(B, workers, G, D);
-    const char *ws = reinterpret_cast<const char *>(a.ws_acc);
-    const int *pre = reinterpret_cast<const int *>(ws + lay.pre);
-    const int nt = pre[b + 1] - pre[b];
-    __half *out = static_cast<__half *>(a.out) + static_cast<size_t>(warp) * D + lane * E;
-    if (nt == 0) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) out[e] = __float2half_rn(0.f);
-        if (lane == 0 && a.lse_out) a.lse_out[warp] = -INFINITY;
-        return;
+    // every tile is consumed: the ring is free for the merges
+    for (int i = 0; i < pend_n; ++i) {
+        if (!merge(pend_b[i], pend_j[i], pend_x0[i], pend_nt[i])) {
+            if (lane == 0) flag_error(a.err, PKV_ERRBIT_TIMEOUT);
+            return;
+        }
     }
-    const long long T = static_cast<long long>(Hk) * pre[B];
-    const long long x0 = static_cast<long long>(Hk) * pre[b] + static_cast<long long>(j) * nt;
-    const long long x1 = x0 + nt - 1;
-    // worker holding unit x: the largest w with w*T/W <= x
-    auto owner = [&](long long x) { return static_cast<int>(((x + 1) * workers + T - 1) / T - 1); };
-    const int wf = owner(x0);
-    const int wl = owner(x1);
-    if (wf == wl) return;  // written whole by one worker
-    const bool wf_starts_here = (static_cast<long long>(wf) * T / workers) == x0;
-    const int np = wl - wf + 1;
-    const float *pm = reinterpret_cast<const float *>(ws + lay.m);
-    const float *pl = reinterpret_cast<const float *>(ws + lay.l);
-    const float *pacc = reinterpret_cast<const float *>(ws + lay.acc);
-    auto piece = [&](int i) {
-        const int wk = wf + i;
-        const int slot = (i == 0 && !wf_starts_here) ? 1 : 0;
-        return (static_cast<size_t>(wk) * 2 + slot) * G + gi;
-    };
-    // pieces with m = -inf (empty workers, skipped blocks) carry no weight
-    float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) M = fmaxf(M, pm[piece(i)]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (M == -INFINITY) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) out[e] = __float2half_rn(0.f);
-        if (lane == 0 && a.lse_out) a.lse_out[warp] = -INFINITY;
-        return;
-    }
-    float tot = 0.f;
-    for (int i = lane; i < np; i += 32) {
-        const size_t pi = piece(i);
-        const float mi = pm[pi];
-        if (mi != -INFINITY) tot = fmaf(exp2f(mi - M), pl[pi], tot);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int i = 0; i < np; ++i) {
-        const size_t pi = piece(i);
-        const float mi = pm[pi];
-        if (mi == -INFINITY) continue;
-        const float wgt = exp2f(mi - M);
-        const float *src = pacc + pi * D + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, src[e], acc[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = __float2half_rn(acc[e] / tot);
-    if (lane == 0 && a.lse_out) a.lse_out[warp] = (M + log2f(tot)) * kLn2b;
 }
 
 template <int D, int G>
@@ -427,6 +437,10 @@ int bal_ctas_per_sm(int B) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bal_smem<D, G>(kMaxSeqsBalanced))) != cudaSuccess)
         return 0;
+    // the grid is sized to fill every SM once: ask for the whole carve-out
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreadsB, smem) != cudaSuccess)
         return 0;
@@ -439,13 +453,8 @@ cudaError_t launch_bal_t(const DecodeArgs &a, const BalancedPlan &plan, const CU
                          const CUtensorMap &tv, cudaStream_t stream) {
     auto kern = decode_balanced_kernel<D, G>;
     if (bal_ctas_per_sm<D, G>(a.num_seqs) <= 0) return cudaErrorInvalidConfiguration;
-    cudaError_t e = launch_pdl(kern, dim3(plan.ctas), dim3(kThreadsB),
-                               bal_smem<D, G>(a.num_seqs), stream, a, tk, tv, plan.workers);
-    if (e != cudaSuccess) return e;
-    const long long warps = static_cast<long long>(a.num_seqs) * a.n_q_heads;
-    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    return launch_pdl(balanced_merge_kernel<D, G>, dim3(blocks), dim3(256), 0, stream, a,
-                      plan.workers);
+    return launch_pdl(kern, dim3(plan.ctas), dim3(kThreadsB), bal_smem<D, G>(a.num_seqs), stream,
+                      a, tk, tv, plan.workers);
 }
 
 int sm_count_cached() {
@@ -485,16 +494,18 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
 #undef PKV_BAL_OCC
     const int sms = sm_count_cached();
     if (per_sm <= 0 || sms <= 0) return false;
-    // upper bound on the units; at least 2 tiles per warp on average
+    // units must fit 32-bit arithmetic: Hk * B * tiles per sequence
     const long long t_max = static_cast<long long>(n_kv_heads) * num_seqs *
                             ((static_cast<long long>(max_len) + kMmaTile - 1) / kMmaTile);
+    if (t_max >= (1LL << 31)) return false;
     long long ctas = static_cast<long long>(sms) * per_sm;
-    const long long need = (t_max + 2 * kW - 1) / (2 * kW);
+    const long long need = (t_max + 2 * kW - 1) / (2 * kW);  // >= 2 tiles per warp on average
     if (need < ctas) ctas = need;
+    if (ctas * kW > kMaxWorkers) ctas = kMaxWorkers / kW;
     if (ctas < 1) ctas = 1;
     plan->ctas = static_cast<int>(ctas);
     plan->workers = plan->ctas * kW;
-    plan->ws_bytes = bal_layout(num_seqs, plan->workers, G, head_dim).total;
+    plan->ws_bytes = bal_ws_bytes(plan->workers, G, head_dim);
     return true;
 }
 

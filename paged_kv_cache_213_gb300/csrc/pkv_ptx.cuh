@@ -176,3 +176,20 @@ __device__ __forceinline__ void allow_dependent_launch() {
 }
 
 }  // namespace pkv
+
+namespace pkv {
+
+// atomicAdd with acquire-release semantics at GPU scope: the release covers
+// every write ordered before it (cumulativity), e.g. other lanes' writes made
+// visible to this lane by __syncwarp(); the acquire orders later reads.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void store_relaxed_gpu(int *p, int v) {
+    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+}  // namespace pkv

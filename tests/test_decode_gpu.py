@@ -280,3 +280,32 @@ def test_balanced_split_shapes(lens_kind):
     fin = np.isfinite(ref["lse"])
     assert np.max(np.abs(g["lse"][fin] - ref["lse"][fin])) <= 1e-4
     assert np.all(np.isneginf(g["lse"][~fin]))
+
+
+def test_balanced_workspace_reuse_across_plans():
+    """One zero-filled workspace serves calls with different shapes in a row:
+    the per-segment arrival counters are left at zero by every call."""
+    batches = [wl.workload(2, poison=True), wl.workload(3, poison=True),
+               wl.make_batch("r", [5000, 17, 3000], 32, 8, 128, 16,
+                             np.random.default_rng(9), append=False, poison=True)]
+    sizes = []
+    for bt in batches:
+        P, ws = pkv.decode_plan(bt.num_seqs, bt.n_q_heads, bt.n_kv_heads, bt.head_dim,
+                                bt.block_size, bt.max_blocks_per_seq, bt.max_context_len, 0)
+        assert P == 0
+        sizes.append(ws)
+    work = torch.zeros(max(sizes), dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for bt in batches:
+            dev = to_dev(bt)
+            if bt.has_append:
+                pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"],
+                                    dev["k_cache"], dev["v_cache"])
+            out = pkv.paged_decode_attention(
+                dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                dev["context_lens"], bt.scale, bt.n_q_heads, bt.n_kv_heads, bt.head_dim,
+                bt.block_size, max_context_len=bt.max_context_len, workspace=work)
+            ref = oracle_step(bt)
+            assert_close(out.cpu().numpy(), ref["out"], what=f"{bt.name} rep {rep}")
+    counters = work[: 16384 * 4].view(torch.int32)
+    assert int(counters.abs().sum()) == 0
