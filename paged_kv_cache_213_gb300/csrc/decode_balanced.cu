@@ -1,8 +1,8 @@
 // decode_balanced.cu -- paged decode attention with the work split evenly
 // over warps (the default tensor-core path).
 //
-// The work of one call is the list of (sequence b, KV head j, 16-token tile t)
-// units, ordered b, then j, then t: T units in all.  The W warps of the grid
+// The work of one call is the list of (KV head j, sequence b, 16-token tile t)
+// units, ordered j, then b, then t: T units in all.  The W warps of the grid
 // (W = 4 x number of CTAs, sized to fill every SM once) take consecutive
 // ranges of U = ceil(T / W) units each, so every warp moves the same number of
 // K/V bytes whatever the mix of context lengths.  A warp streams its range
@@ -77,31 +77,37 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b, bool flag
     return L;
 }
 
-// Position of unit x: the sequence b whose units contain it, the KV head j,
-// the tile t.  pre[] is the tile prefix (units of b: Hk * pre[b] ..).
+// Units are ordered KV head j, then sequence b, then tile t, so that
+// sequences holding the same physical prefix blocks (forked siblings, shared
+// prompts) sit next to each other and their warps reach the shared blocks at
+// about the same time (the later reads then hit L2).  pre[] is the tile
+// prefix over sequences; TB = pre[B] units per KV head.
 struct Cursor {
     int b, j, t;
 };
 
-__device__ __forceinline__ Cursor locate(int x, const int *pre, int B, int Hk) {
-    int lo = 0, hi = B - 1;  // largest b with Hk * pre[b] <= x
+__device__ __forceinline__ Cursor locate(int x, const int *pre, int B) {
+    const int TB = pre[B];
+    const int j = x / TB;
+    const int r = x - j * TB;
+    int lo = 0, hi = B - 1;  // largest b with pre[b] <= r (it has tiles)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (Hk * pre[mid] <= x) lo = mid; else hi = mid - 1;
+        if (pre[mid] <= r) lo = mid; else hi = mid - 1;
     }
-    const int r = x - Hk * pre[lo];
-    const int nt = pre[lo + 1] - pre[lo];
-    return Cursor{lo, r / nt, r % nt};
+    return Cursor{lo, j, r - pre[lo]};
 }
 
-__device__ __forceinline__ void advance(Cursor &c, const int *pre, int B, int Hk) {
+__device__ __forceinline__ void advance(Cursor &c, const int *pre, int B) {
     if (++c.t < pre[c.b + 1] - pre[c.b]) return;
     c.t = 0;
-    if (++c.j < Hk) return;
-    c.j = 0;
     do {
         ++c.b;
     } while (c.b < B && pre[c.b + 1] == pre[c.b]);
+    if (c.b < B) return;
+    ++c.j;
+    c.b = 0;
+    while (c.b < B && pre[c.b + 1] == pre[c.b]) ++c.b;
 }
 
 template <int D, int G>
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kThreadsB)
 
     unsigned char *my_pipe = smem + warp * kS * C::SLOT_BYTES;
     unsigned char *my_q = qslots + warp * kS * C::Q_BYTES;
-    Cursor pc = locate(w0, s_pre, B, Hk);  // producer cursor
+    Cursor pc = locate(w0, s_pre, B);  // producer cursor
     Cursor cc = pc;                        // consumer cursor
     int prev_seg_p = -1;
 
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kThreadsB)
     auto load_ids = [&](int chunk_no) -> int {
         const int kk = chunk_no * 32 + lane;
         if (kk >= n) return -1;
-        const Cursor c = locate(w0 + kk, s_pre, B, Hk);
+        const Cursor c = locate(w0 + kk, s_pre, B);
         return a.block_tables[static_cast<size_t>(c.b) * a.max_blocks_per_seq +
                               (c.t * kMmaTile) / bs];
     };
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kThreadsB)
     // All lanes call (the cursor bookkeeping is warp-uniform); lane 0 issues.
     auto issue = [&](int k) {
         const int slot = k % kS;
-        const int seg = pc.b * Hk + pc.j;
+        const int seg = pc.j * B + pc.b;
         const bool newseg = seg != prev_seg_p;
         prev_seg_p = seg;
         if (k > 0 && (k & 31) == 0) {
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kThreadsB)
                                   (static_cast<size_t>(pc.b) * H + static_cast<size_t>(pc.j) * G) * D,
                               C::Q_BYTES, bar);
         }
-        advance(pc, s_pre, B, Hk);
+        advance(pc, s_pre, B);
     };
 
     const int pro = n < kS ? n : kS;
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(kThreadsB)
             }
         }
         __syncwarp();  // the record's stores, all lanes, before lane 0's release
-        const int x0 = Hk * s_pre[pb] + pj * nt;  // the segment's units [x0, x0 + nt)
+        const int x0 = pj * s_pre[B] + s_pre[pb];  // the segment's units [x0, x0 + nt)
         const int wf = x0 / U;
         const int wl = (x0 + nt - 1) / U;
         int old = 0;
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(kThreadsB)
             timed_out = true;
             break;
         }
-        const int seg = cc.b * Hk + cc.j;
+        const int seg = cc.j * B + cc.b;
         if (seg != cur_seg) {
             if (cur_seg >= 0) flush();
 #pragma unroll
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(kThreadsB)
             issue(k + kS);
             ++issued;
         }
-        advance(cc, s_pre, B, Hk);
+        advance(cc, s_pre, B);
     }
     if (timed_out) {
         if (lane == 0) {
