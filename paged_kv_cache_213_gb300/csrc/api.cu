@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "pagedkv.h"
+#include "pagedkv_blocks.h"
 #include "pkv_internal.h"
 
 namespace {
@@ -222,6 +223,25 @@ int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits
     return host == 0 ? PKV_OK : PKV_ERR_INDEX;
 }
 
+int paged_kv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst,
+                         const int32_t *tokens, int num_copies, int n_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, int32_t *err_word,
+                         void *cuda_stream) {
+    if (num_copies < 0 || n_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 ||
+        block_size <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_copies == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src || !dst || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(src, 4) || !aligned(dst, 4) || (tokens && !aligned(tokens, 4)) ||
+        (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    const cudaError_t e =
+        pkv::launch_copy_blocks(k_cache, v_cache, src, dst, tokens, num_copies, n_kv_heads,
+                                head_dim, block_size, num_blocks, err_word,
+                                static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 const char *paged_kv_status_string(int status) {
     switch (status) {
         case PKV_OK: return "ok";
@@ -230,6 +250,7 @@ const char *paged_kv_status_string(int status) {
         case PKV_ERR_WORKSPACE: return "workspace missing or too small";
         case PKV_ERR_CUDA: return "CUDA runtime error";
         case PKV_ERR_INDEX: return "device flagged a bad index";
+        case PKV_ERR_OUT_OF_BLOCKS: return "no free block in the pool";
         default: return "unknown status";
     }
 }

@@ -56,3 +56,51 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace pkv
+
+// Copy-on-write block copy ("Distributed LLM Inference Serving Platform",
+// Lab 1 worked solution: the fresh tail block receives the shared tail's
+// tokens).  One thread moves one 16-byte vector of K and one of V.
+namespace pkv {
+namespace {
+
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                       const int32_t *__restrict__ src, const int32_t *__restrict__ dst,
+                       const int32_t *__restrict__ tokens, int num_copies, int n_kv_heads,
+                       int chunks, int block_size, long long num_blocks, int32_t *err) {
+    const long long per_copy = static_cast<long long>(n_kv_heads) * block_size * chunks;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= per_copy * num_copies) return;
+    const int i = static_cast<int>(idx / per_copy);
+    const long long r = idx % per_copy;  // (head, row, chunk) inside the block
+    const int row = static_cast<int>((r / chunks) % block_size);
+    const int s = src[i];
+    const int d = dst[i];
+    const int n = tokens ? tokens[i] : block_size;
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks || n < 0 || n > block_size) {
+        if (r == 0) flag_error(err, PKV_ERRBIT_SLOT);
+        return;
+    }
+    if (row >= n) return;
+    const long long block_vecs = per_copy;  // uint4 per (block, all heads)
+    k_cache[d * block_vecs + r] = k_cache[s * block_vecs + r];
+    v_cache[d * block_vecs + r] = v_cache[s * block_vecs + r];
+}
+
+}  // namespace
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
+                               const int32_t *dst, const int32_t *tokens, int num_copies,
+                               int n_kv_heads, int head_dim, int block_size, long long num_blocks,
+                               int32_t *err, cudaStream_t stream) {
+    const int chunks = head_dim / 8;
+    const long long total = static_cast<long long>(num_copies) * n_kv_heads * block_size * chunks;
+    if (total == 0) return cudaSuccess;
+    const long long blocks = (total + 255) / 256;
+    copy_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src, dst, tokens,
+        num_copies, n_kv_heads, chunks, block_size, num_blocks, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -76,6 +76,10 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts);
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
+                               const int32_t *dst, const int32_t *tokens, int num_copies,
+                               int n_kv_heads, int head_dim, int block_size, long long num_blocks,
+                               int32_t *err, cudaStream_t stream);
 // Returns cudaErrorInvalidValue for a (head_dim, group) pair with no kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 bool decode_supported(int head_dim, int group);
