@@ -57,6 +57,8 @@ def parse_args(argv=None):
                     help="steps captured per CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU-oracle sample length for cpu_baseline")
+    ap.add_argument("--prefix-shared", action="store_true",
+                    help="use the prefix-aware entry point (workloads with shared prefixes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -181,7 +183,7 @@ def workload_bytes(batch):
 
 def source_sha():
     h = hashlib.sha256()
-    for name in ("decode.cu", "decode_mma.cu", "pkv_ptx.cuh"):
+    for name in ("decode_balanced.cu", "mma_tile.cuh", "pkv_ptx.cuh", "shared_prefix.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_213_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -295,8 +297,16 @@ def run_ours(args):
     mcl = batch.max_context_len
     P, ws_bytes = pkv.decode_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
                                   args.partition)
+    # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
+    launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 and P > 0 else 0)
+    groups = None
+    if args.prefix_shared and batch.meta.get("shared"):
+        offs, pref, gmax, pmax = wl.prefix_groups(batch)
+        groups = (t(offs), t(pref), gmax, pmax)
+        ws_bytes = pkv.prefix_shared_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
+                                          len(pref), gmax, pmax)
+        launches_per_step = (1 if has_append else 0) + 2
     work = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 else 0)
 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush_w = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
@@ -312,6 +322,11 @@ def run_ours(args):
             pkv.paged_kv_append(kn, vn, sm, kc, vc, err_word=err)
 
     def attend():
+        if groups is not None:
+            pkv.paged_decode_attention_prefix_shared(
+                q, kc, vc, bt, cl, batch.scale, H, Hk, D, bs, groups[0], groups[1], groups[2],
+                groups[3], max_context_len=mcl, out=out, workspace=work, err_word=err)
+            return
         pkv.paged_decode_attention(q, kc, vc, bt, cl, batch.scale, H, Hk, D, bs,
                                    max_context_len=mcl, partition_tokens=P, out=out,
                                    workspace=work if ws_bytes > 0 else None, err_word=err)
@@ -472,6 +487,7 @@ def run_ours(args):
             "parallelism": f"replicas x{world}",
             "decode_kernel": os.environ.get("PKV_DECODE_KERNEL",
                                             "auto (tensor-core kernel when block_size % 16 == 0)"),
+            "prefix_shared": groups is not None,
         },
         "steps_per_sec": round(1e3 / step_ms, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),

@@ -170,6 +170,49 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int32_t *err_word, void *cuda_stream);
 
 /*
+ * Prefix-aware (cascade) decode attention ("Distributed LLM Inference Serving
+ * Platform", section 2 and Lab 1: prompt blocks shared by parallel
+ * completions; section 5.1 Ingestion: a cached common prefix referenced by
+ * several requests).  Same result as paged_decode_attention, but the leading
+ * blocks that a group of sequences shares are read from HBM once per chunk
+ * of up to 64 / (n_q_heads / n_kv_heads) members instead of once per member:
+ * a first pass attends every member's queries over the shared tiles, the
+ * balanced pass attends each member's private suffix and merges the two by
+ * log-sum-exp.
+ *
+ *  group_offsets      device int32 [num_groups + 1], non-decreasing, with
+ *                     group_offsets[0] = 0 and group_offsets[num_groups] =
+ *                     num_seqs: group i is sequences [offsets[i],
+ *                     offsets[i+1])
+ *  group_prefix_lens  device int32 [num_groups]: tokens whose blocks every
+ *                     member of the group holds at the same logical index as
+ *                     the group's first sequence (same physical block ids).
+ *                     The shared pass uses floor(min(prefix, shortest member)
+ *                     / 16) whole tiles; the rest is private.  Groups of one
+ *                     sequence, or with prefix 0, have no shared pass.
+ *  max_group_size, max_prefix_len   host upper bounds (grid sizing)
+ * Other arguments as paged_decode_attention (partition_tokens is implied:
+ * the balanced split).  Needs block_size a multiple of 16 and at most 2048
+ * sequences (PKV_ERR_UNSUPPORTED otherwise).  If a member's table does not
+ * hold the group's first sequence's block ids for the shared prefix, that
+ * member's result uses the first sequence's blocks there.
+ * paged_decode_prefix_shared_plan gives the workspace bytes; the workspace
+ * must be zero-filled before first use, as for the balanced split.
+ */
+int paged_decode_prefix_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int block_size, int max_blocks_per_seq, int max_context_len,
+                                    int num_groups, int max_group_size, int max_prefix_len,
+                                    size_t *workspace_bytes_out);
+int paged_decode_attention_prefix_shared(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads, int n_kv_heads,
+    int head_dim, int block_size, int max_context_len, const int32_t *group_offsets,
+    const int32_t *group_prefix_lens, int num_groups, int max_group_size, int max_prefix_len,
+    void *workspace, size_t workspace_bytes, float *lse_out, int32_t *err_word,
+    void *cuda_stream);
+
+/*
  * Allocation-free variant of paged_decode_attention.  The pages have no
  * counterpart to this call.  It serves callers that cannot allocate device
  * memory and so cannot supply the split-K workspace: an operator running

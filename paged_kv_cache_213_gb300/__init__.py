@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     library,
     library_path,
     paged_decode_attention,
+    paged_decode_attention_prefix_shared,
     paged_kv_append,
+    prefix_shared_plan,
     status_string,
 )

@@ -212,6 +212,143 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+struct SharedPlan {
+    Plan base;  // the balanced split of the private suffixes
+    int chunks, parts, part_tiles, warps;
+    size_t sh_acc, sh_m, sh_l, total;
+};
+
+int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                     int max_blocks_per_seq, int max_context_len, int num_groups,
+                     int max_group_size, int max_prefix_len, SharedPlan *sp) {
+    if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0) return PKV_ERR_INVALID_ARG;
+    if (pkv::kernel_override() != 0) return PKV_ERR_UNSUPPORTED;
+    int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                       max_context_len, 0, &sp->base);
+    if (rc != PKV_OK) return rc;
+    if (!sp->base.balanced) return PKV_ERR_UNSUPPORTED;
+    const int g = n_q_heads / n_kv_heads;
+    const int mpw = pkv::shared_members_per_warp(g);
+    const int max_tiles =
+        (max_prefix_len < sp->base.max_len ? max_prefix_len : sp->base.max_len) / 16;
+    // warps per CTA: those the largest group needs, at most shared_max_warps()
+    const int need_w = max_group_size > 0 ? (max_group_size + mpw - 1) / mpw : 1;
+    sp->warps = need_w < pkv::shared_max_warps() ? need_w : pkv::shared_max_warps();
+    const int mpc = sp->warps * mpw;
+    sp->chunks = max_group_size > 0 ? (max_group_size + mpc - 1) / mpc : 1;
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    const int per_sm = pkv::shared_ctas_per_sm(head_dim, g, sp->warps);
+    if (per_sm <= 0) return PKV_ERR_CUDA;
+    // one wave of CTAs over the (group chunk, KV head) pairs, at least 4 tiles each
+    const long long pairs =
+        static_cast<long long>(num_groups > 0 ? num_groups : 1) * sp->chunks * n_kv_heads;
+    long long parts = (static_cast<long long>(per_sm) * sms) / pairs;
+    const long long max_parts = max_tiles > 4 ? max_tiles / 4 : 1;
+    if (parts > max_parts) parts = max_parts;
+    if (parts < 1) parts = 1;
+    if (parts > 65535) parts = 65535;
+    sp->part_tiles = max_tiles > 0 ? static_cast<int>((max_tiles + parts - 1) / parts) : 1;
+    sp->parts = max_tiles > 0 ? (max_tiles + sp->part_tiles - 1) / sp->part_tiles : 1;
+    if (static_cast<long long>(num_groups) * sp->chunks > 2147483647LL) return PKV_ERR_UNSUPPORTED;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t rows = static_cast<size_t>(num_seqs) * n_q_heads * sp->parts;
+    sp->sh_acc = up(sp->base.ws_bytes);
+    sp->sh_m = sp->sh_acc + up(rows * head_dim * 4);
+    sp->sh_l = sp->sh_m + up(rows * 4);
+    sp->total = sp->sh_l + up(rows * 4);
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_decode_prefix_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int block_size, int max_blocks_per_seq, int max_context_len,
+                                    int num_groups, int max_group_size, int max_prefix_len,
+                                    size_t *workspace_bytes_out) {
+    SharedPlan sp{};
+    const int rc = make_shared_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                    max_blocks_per_seq, max_context_len, num_groups,
+                                    max_group_size, max_prefix_len, &sp);
+    if (rc == PKV_OK && workspace_bytes_out) *workspace_bytes_out = sp.total;
+    return rc;
+}
+
+int paged_decode_attention_prefix_shared(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads, int n_kv_heads,
+    int head_dim, int block_size, int max_context_len, const int32_t *group_offsets,
+    const int32_t *group_prefix_lens, int num_groups, int max_group_size, int max_prefix_len,
+    void *workspace, size_t workspace_bytes, float *lse_out, int32_t *err_word,
+    void *cuda_stream) {
+    if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (num_groups > 0 && (!group_offsets || !group_prefix_lens || !aligned(group_offsets, 4) ||
+                           !aligned(group_prefix_lens, 4)))
+        return PKV_ERR_INVALID_ARG;
+    SharedPlan sp{};
+    int rc = make_shared_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                              max_blocks_per_seq, max_context_len, num_groups, max_group_size,
+                              max_prefix_len, &sp);
+    if (rc != PKV_OK) return rc;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+        (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sp.total || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
+        return PKV_ERR_UNSUPPORTED;
+    char *base = static_cast<char *>(workspace);
+    pkv::DecodeArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.ws_acc = static_cast<float *>(workspace);
+    a.lse_out = lse_out;
+    a.err = err_word;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.max_context_len = sp.base.max_len;
+    a.partition_tokens = 0;
+    a.max_parts = 1;
+    a.group_offsets = group_offsets;
+    a.group_prefix = group_prefix_lens;
+    a.num_groups = num_groups;
+    a.sh_chunks = sp.chunks;
+    a.sh_parts = sp.parts;
+    a.sh_part_tiles = sp.part_tiles;
+    a.sh_warps = sp.warps;
+    a.sh_acc = reinterpret_cast<float *>(base + sp.sh_acc);
+    a.sh_m = reinterpret_cast<float *>(base + sp.sh_m);
+    a.sh_l = reinterpret_cast<float *>(base + sp.sh_l);
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    cudaError_t e = cudaSuccess;
+    if (num_groups > 0) e = pkv::launch_decode_shared(a, stream);
+    if (e == cudaSuccess) e = pkv::launch_decode_balanced(a, sp.base.bal, stream);
+    if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits_out) {
     if (!err_word) return PKV_ERR_INVALID_ARG;
     int32_t host = 0;

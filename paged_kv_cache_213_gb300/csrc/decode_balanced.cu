@@ -4,8 +4,8 @@
 // The work of one call is the list of (KV head j, sequence b, 16-token tile t)
 // units, ordered j, then b, then t: T units in all.  The W warps of the grid
 // (W = 4 x number of CTAs, sized to fill every SM once) take consecutive
-// ranges of U = ceil(T / W) units each, so every warp moves the same number of
-// K/V bytes whatever the mix of context lengths.  A warp streams its range
+// ranges of U = max(4, ceil(T / W)) units each, so every working warp moves the
+// same number of K/V bytes whatever the mix of context lengths.  A warp streams its range
 // through its own ring of TMA-loaded tiles, carrying the online-softmax state
 // of the current (b, j) "segment".  A segment that ends inside the range is
 // written out directly.  A segment cut by range boundaries leaves one partial
@@ -32,6 +32,7 @@
 #include "pagedkv.h"
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
+#include "shared_prefix.cuh"
 
 namespace pkv {
 namespace {
@@ -44,6 +45,7 @@ constexpr int kS = PKV_BAL_STAGES;  // ring stages per warp
 constexpr int kThreadsB = kW * 32;
 constexpr int kMaxSeqsBalanced = 2048;
 constexpr int kMaxWorkers = 16384;  // size of the counter region
+constexpr int kMinUnits = 4;        // fewest units a working warp takes
 constexpr float kLn2b = 0.69314718055994531f;
 
 template <int D, int G>
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(kThreadsB)
     unsigned char *qslots = smem + C::PIPE_BYTES;
     int *s_pre = reinterpret_cast<int *>(qslots + C::QS_BYTES);  // [B + 1]
     int *s_len = s_pre + a.num_seqs + 1;                          // [B]
+    int *s_skip = s_len + a.num_seqs;  // [B] tiles left to the shared-prefix pass
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -144,12 +147,26 @@ __global__ void __launch_bounds__(kThreadsB)
     const int chunk = (B + kThreadsB - 1) / kThreadsB;
     const int c0 = min(B, tid * chunk);
     const int c1 = min(B, c0 + chunk);
-    int local = 0;
     for (int b = c0; b < c1; ++b) {
-        const int L = clamped_len(a, b, blockIdx.x == 0);
-        s_len[b] = L;
-        local += (L + kMmaTile - 1) / kMmaTile;
+        s_len[b] = clamped_len(a, b, blockIdx.x == 0);
+        s_skip[b] = 0;
     }
+    if (a.num_groups > 0) {
+        __syncthreads();
+        // members of a prefix-shared group leave the shared tiles to that pass
+        for (int gi = tid; gi < a.num_groups; gi += kThreadsB) {
+            const int f = max(0, min(B, a.group_offsets[gi]));
+            const int e = max(f, min(B, a.group_offsets[gi + 1]));
+            if (e - f < 2) continue;
+            int mn = INT_MAX;
+            for (int b = f; b < e; ++b) mn = min(mn, s_len[b]);
+            const int st = shared_tiles(a, gi, mn);
+            for (int b = f; b < e; ++b) s_skip[b] = st;
+        }
+        __syncthreads();
+    }
+    int local = 0;
+    for (int b = c0; b < c1; ++b) local += (s_len[b] + kMmaTile - 1) / kMmaTile - s_skip[b];
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -172,24 +189,41 @@ __global__ void __launch_bounds__(kThreadsB)
     int run = base + incl - local;
     for (int b = c0; b < c1; ++b) {
         s_pre[b] = run;
-        run += (s_len[b] + kMmaTile - 1) / kMmaTile;
+        run += (s_len[b] + kMmaTile - 1) / kMmaTile - s_skip[b];
     }
     if (tid == kThreadsB - 1) s_pre[B] = base + incl;
     __syncthreads();
 
-    // empty sequences: out = 0, lse = -inf (sequences spread over the CTAs)
+    // Sequences without private tiles (sequences spread over the CTAs): empty
+    // ones get out = 0, lse = -inf; the others are the shared pass's result.
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        if (s_len[b] != 0) continue;
+        if (s_pre[b + 1] != s_pre[b]) continue;
         __half *ob = static_cast<__half *>(a.out) + static_cast<size_t>(b) * H * D;
-        for (int i = tid; i < H * D; i += kThreadsB) ob[i] = __float2half_rn(0.f);
-        if (a.lse_out)
-            for (int h = tid; h < H; h += kThreadsB) a.lse_out[static_cast<size_t>(b) * H + h] = -INFINITY;
+        for (int i = tid; i < H * D; i += kThreadsB) {
+            const int h = i / D;
+            float M = -INFINITY, Ls = 0.f, A = 0.f;
+            if (s_skip[b] > 0) {
+                const size_t r0 = (static_cast<size_t>(b) * H + h) * a.sh_parts;
+                for (int pp = 0; pp < a.sh_parts; ++pp) M = fmaxf(M, a.sh_m[r0 + pp]);
+                for (int pp = 0; pp < a.sh_parts && M != -INFINITY; ++pp) {
+                    const float mp = a.sh_m[r0 + pp];
+                    if (mp == -INFINITY) continue;
+                    const float wgt = exp2f(mp - M);
+                    Ls = fmaf(wgt, a.sh_l[r0 + pp], Ls);
+                    A = fmaf(wgt, a.sh_acc[(r0 + pp) * D + i % D], A);
+                }
+            }
+            ob[i] = __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
+            if (a.lse_out && i % D == 0)
+                a.lse_out[static_cast<size_t>(b) * H + h] = Ls > 0.f ? (M + log2f(Ls)) * kLn2b : -INFINITY;
+        }
     }
 
     // --- this warp's range of units: [w * U, (w + 1) * U) clipped to T
     const int w = blockIdx.x * kW + warp;
     const int T = Hk * s_pre[B];
-    const int U = (T + workers - 1) / workers;
+    // at least kMinUnits units per warp: short segments then stay whole
+    const int U = max(kMinUnits, (T + workers - 1) / workers);
     const int w0 = static_cast<int>(min(static_cast<long long>(T), static_cast<long long>(w) * U));
     const int n = min(T, w0 + U) - w0;
     if (n <= 0) return;  // no CTA-wide barriers below
@@ -208,7 +242,7 @@ __global__ void __launch_bounds__(kThreadsB)
         if (kk >= n) return -1;
         const Cursor c = locate(w0 + kk, s_pre, B);
         return a.block_tables[static_cast<size_t>(c.b) * a.max_blocks_per_seq +
-                              (c.t * kMmaTile) / bs];
+                              ((c.t + s_skip[c.b]) * kMmaTile) / bs];
     };
     int ids_cur = load_ids(0);
     int ids_next = load_ids(1);
@@ -226,7 +260,7 @@ __global__ void __launch_bounds__(kThreadsB)
         const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
         if (lane == 0) {
             uint64_t *bar = &full_bar[warp][slot];
-            const int tok0 = pc.t * kMmaTile;
+            const int tok0 = (pc.t + s_skip[pc.b]) * kMmaTile;
             const bool ok = id >= 0 && id < a.num_blocks;
             if (!ok) flag_error(a.err, PKV_ERRBIT_BLOCK_ID);
             s_ok[warp][slot] = ok;
@@ -268,6 +302,37 @@ __global__ void __launch_bounds__(kThreadsB)
     auto write_out = [&](int b, int j, float fm, float fl) {
         if (g >= G) return;
         const size_t bh = static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + g;
+        if (s_skip[b] > 0) {  // fold in the shared-prefix partial states
+            const size_t r0 = bh * a.sh_parts;
+            float M = fm;
+#pragma unroll 4
+            for (int pp = 0; pp < a.sh_parts; ++pp) M = fmaxf(M, a.sh_m[r0 + pp]);
+            const float so = M == -INFINITY ? 0.f : exp2f(fm - M);  // 0: no private part
+            fl *= so;
+#pragma unroll
+            for (int nb = 0; nb < C::NB_D; ++nb) {
+                o[nb][0] *= so;
+                o[nb][1] *= so;
+            }
+#pragma unroll 4
+            for (int pp = 0; pp < a.sh_parts; ++pp) {
+                const float mp = a.sh_m[r0 + pp];
+                const float lp = a.sh_l[r0 + pp];
+                const float2 *src = reinterpret_cast<const float2 *>(a.sh_acc + (r0 + pp) * D);
+                float2 v[C::NB_D];
+#pragma unroll
+                for (int nb = 0; nb < C::NB_D; ++nb) v[nb] = src[nb * 4 + tq];
+                if (mp == -INFINITY) continue;
+                const float sn = exp2f(mp - M);
+                fl = fmaf(lp, sn, fl);
+#pragma unroll
+                for (int nb = 0; nb < C::NB_D; ++nb) {
+                    o[nb][0] = fmaf(v[nb].x, sn, o[nb][0]);
+                    o[nb][1] = fmaf(v[nb].y, sn, o[nb][1]);
+                }
+            }
+            fm = M;
+        }
         const float inv = fl > 0.f ? 1.f / fl : 0.f;
         __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
 #pragma unroll
@@ -398,7 +463,8 @@ __global__ void __launch_bounds__(kThreadsB)
         last_t = cc.t;
         unsigned char *ks = my_pipe + slot * C::SLOT_BYTES;
         unsigned char *vs = ks + C::TILE_BYTES;
-        const int n_valid = s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - cc.t * kMmaTile) : 0;
+        const int n_valid =
+            s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - (cc.t + s_skip[cc.b]) * kMmaTile) : 0;
         mma_tile<D>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
         __syncwarp();
         if (k + kS < n) {
@@ -428,7 +494,7 @@ __global__ void __launch_bounds__(kThreadsB)
 template <int D, int G>
 size_t bal_smem(int B) {
     using C = BalCfg<D, G>;
-    return 1024 + C::PIPE_BYTES + C::QS_BYTES + (2 * static_cast<size_t>(B) + 1) * 4;
+    return 1024 + C::PIPE_BYTES + C::QS_BYTES + (3 * static_cast<size_t>(B) + 1) * 4;
 }
 
 template <int D, int G>

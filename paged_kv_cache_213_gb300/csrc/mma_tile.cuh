@@ -143,3 +143,91 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
 }
 
 }  // namespace pkv
+
+namespace pkv {
+
+// Both halves of the 16-row A tile carry queries: row g ("lo") and row g+8
+// ("hi") of lane 4g+tq, each with its own online-softmax state.  Used where
+// one K/V tile serves several sequences' queries at once (shared prefixes).
+// All 16 rows of the tile take part (a shared prefix is made of full tiles).
+template <int D>
+__device__ __forceinline__ void mma_tile_2rows(const unsigned char *ks, const unsigned char *vs,
+                                               const uint32_t (&qlo)[MmaCfg<D>::NP][4],
+                                               const uint32_t (&qhi)[MmaCfg<D>::NP][4],
+                                               float scale_log2, float (&o)[MmaCfg<D>::NB_D][4],
+                                               float &m_lo, float &l_lo, float &m_hi, float &l_hi,
+                                               int lane) {
+    using C = MmaCfg<D>;
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    float sacc[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+        sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
+        const int t = nb * 8 + g;
+#pragma unroll
+        for (int p = 0; p < C::NP; ++p) {
+            const uint4 kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
+                                                              swz(t, 2 * tq + (p & 1)));
+            const uint32_t a0[4] = {qlo[p][0], qhi[p][0], qlo[p][1], qhi[p][1]};
+            mma_16816(sacc[nb], a0, kw.x, kw.y);
+            const uint32_t a1[4] = {qlo[p][2], qhi[p][2], qlo[p][3], qhi[p][3]};
+            mma_16816(sacc[nb], a1, kw.z, kw.w);
+        }
+    }
+    float mxl = -INFINITY, mxh = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            sacc[nb][e] *= scale_log2;
+            sacc[nb][2 + e] *= scale_log2;
+            mxl = fmaxf(mxl, sacc[nb][e]);
+            mxh = fmaxf(mxh, sacc[nb][2 + e]);
+        }
+    }
+    mxl = fmaxf(mxl, __shfl_xor_sync(0xffffffffu, mxl, 1));
+    mxl = fmaxf(mxl, __shfl_xor_sync(0xffffffffu, mxl, 2));
+    mxh = fmaxf(mxh, __shfl_xor_sync(0xffffffffu, mxh, 1));
+    mxh = fmaxf(mxh, __shfl_xor_sync(0xffffffffu, mxh, 2));
+    const float mnl = fmaxf(m_lo, mxl);
+    const float mnh = fmaxf(m_hi, mxh);
+    const float cl = exp2f(m_lo - mnl);  // 0 while m = -inf
+    const float ch = exp2f(m_hi - mnh);
+    float pl[2][2], ph[2][2], sl = 0.f, sh = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            pl[nb][e] = exp2f(sacc[nb][e] - mnl);
+            ph[nb][e] = exp2f(sacc[nb][2 + e] - mnh);
+            sl += pl[nb][e];
+            sh += ph[nb][e];
+        }
+    l_lo = l_lo * cl + sl;
+    l_hi = l_hi * ch + sh;
+    m_lo = mnl;
+    m_hi = mnh;
+#pragma unroll
+    for (int n = 0; n < C::NB_D; ++n) {
+        o[n][0] *= cl;
+        o[n][1] *= cl;
+        o[n][2] *= ch;
+        o[n][3] *= ch;
+    }
+    const uint32_t pa[4] = {pack_half2(pl[0][0], pl[0][1]), pack_half2(ph[0][0], ph[0][1]),
+                            pack_half2(pl[1][0], pl[1][1]), pack_half2(ph[1][0], ph[1][1])};
+    const int lm = lane >> 3;
+    const int ri = lane & 7;
+    const int vt = ((lm & 1) << 3) + ri;
+#pragma unroll
+    for (int qd = 0; qd < C::NB_D / 2; ++qd) {
+        const int u = 2 * qd + (lm >> 1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
+        mma_16816(o[2 * qd], pa, r0, r1);
+        mma_16816(o[2 * qd + 1], pa, r2, r3);
+    }
+}
+
+}  // namespace pkv

@@ -67,6 +67,17 @@ struct DecodeArgs {
     int max_context_len;          // clamp bound, > 0
     int partition_tokens;         // multiple of 16 and of block_size
     int max_parts;                // ceil(max_context_len / partition_tokens)
+    // prefix-shared groups (num_groups = 0: none)
+    const int32_t *group_offsets; // [num_groups + 1] consecutive ranges of sequences
+    const int32_t *group_prefix;  // [num_groups] shared prefix tokens
+    int num_groups;
+    int sh_chunks;                // CTA chunks per group in the shared pass
+    int sh_parts;                 // partitions of the shared prefix
+    int sh_part_tiles;            // 16-token tiles per partition
+    int sh_warps;                 // warps per shared-pass CTA
+    float *sh_acc;                // [B][H][sh_parts][D] shared-pass partial sums
+    float *sh_m;                  // [B][H][sh_parts]
+    float *sh_l;                  // [B][H][sh_parts]
 };
 
 // Workspace carve-up shared by the planner and the launcher.
@@ -105,5 +116,10 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
                    BalancedPlan *plan);
 cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
                                    cudaStream_t stream);
+// Shared-prefix pass (decode_shared.cu): each warp holds 16 query rows.
+int shared_members_per_warp(int group);
+int shared_max_warps();
+int shared_ctas_per_sm(int head_dim, int group, int warps);
+cudaError_t launch_decode_shared(const DecodeArgs &a, cudaStream_t stream);
 
 }  // namespace pkv

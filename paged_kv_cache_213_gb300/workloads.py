@@ -265,3 +265,33 @@ def stats(batch: PagedBatch) -> dict:
         "step_unique": unique_tokens * per_token + qo + meta + app,
         "step_logical": logical_tokens * per_token + qo + meta + app,
     }
+
+
+def prefix_groups(batch: PagedBatch):
+    """Consecutive-range groups of the batch's shared prefixes, for the
+    prefix-shared entry point: (offsets int32 [G+1], prefix tokens int32 [G],
+    largest group, longest prefix).  Sequences outside any shared group form
+    one-sequence groups with prefix 0."""
+    B = batch.num_seqs
+    member_of = {}
+    for members, n_shared in batch.meta.get("shared", []):
+        ms = sorted(members)
+        if ms != list(range(ms[0], ms[0] + len(ms))):
+            raise ValueError("shared groups must be consecutive sequences")
+        for b in ms:
+            member_of[b] = (ms[0], len(ms), n_shared * batch.block_size)
+    offsets, prefix = [0], []
+    b = 0
+    while b < B:
+        if b in member_of:
+            first, n, tokens = member_of[b]
+            offsets.append(first + n)
+            prefix.append(tokens)
+            b = first + n
+        else:
+            offsets.append(b + 1)
+            prefix.append(0)
+            b += 1
+    sizes = np.diff(offsets)
+    return (np.asarray(offsets, dtype=np.int32), np.asarray(prefix, dtype=np.int32),
+            int(sizes.max()) if sizes.size else 0, int(max(prefix) if prefix else 0))

@@ -1,0 +1,99 @@
+"""Prefix-aware decode attention (shared prefix read once per group chunk)
+against the oracle: the Mistral-shaped mix and the 70B parallel-sampling
+workloads, and edge cases -- prefixes that are not whole tiles, members
+shorter than the prefix, sequences with no private tile, groups larger than
+one CTA chunk, one-sequence groups, every GQA group size and head_dim."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_213_gb300 as pkv
+from gpu_util import assert_close, oracle_step, to_dev
+from paged_kv_cache_213_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.library()
+
+
+def run_shared(batch, groups=None):
+    offs, pref, gmax, pmax = groups if groups is not None else wl.prefix_groups(batch)
+    dev = to_dev(batch)
+    if batch.has_append:
+        pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                            dev["v_cache"])
+    lse = torch.full((batch.num_seqs, batch.n_q_heads), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pkv.paged_decode_attention_prefix_shared(
+        dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+        batch.scale, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size,
+        torch.from_numpy(offs).cuda(), torch.from_numpy(pref).cuda(), gmax, pmax,
+        max_context_len=batch.max_context_len, lse=lse, err_word=err)
+    assert pkv.get_error(err) == 0
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_shared_workloads(cfg):
+    batch = wl.workload(cfg, poison=True)
+    mask = None
+    if cfg == 5:
+        rng = np.random.default_rng(55)
+        mask = np.zeros((batch.num_seqs, batch.n_q_heads), dtype=bool)
+        mask.reshape(-1)[rng.choice(mask.size, 256, replace=False)] = True
+        mask[:4] = True  # one whole group
+    out, lse = run_shared(batch)
+    ref = oracle_step(batch, mask=mask)
+    assert_close(out, ref["out"], mask=mask, what=f"workload {cfg}")
+    sel = mask if mask is not None else np.ones(lse.shape, dtype=bool)
+    assert np.max(np.abs(lse[sel] - ref["lse"][sel])) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_shared_edge_cases(d, G):
+    rng = np.random.default_rng(700 + 10 * d + G)
+    Hk = 2
+    # group A: 5 members, prefix 3 blocks, one member shorter than the prefix
+    # group B: 2 members sharing everything they have (no private tile)
+    # group C: one sequence; group D: 3 members with a prefix that is no whole tile
+    lens = [100, 60, 33, 130, 75, 64, 64, 40, 90, 91, 70]
+    shared = [([0, 1, 2, 3, 4], 3), ([5, 6], 4), ([8, 9, 10], 3)]
+    batch = wl.make_batch("edge", lens, Hk * G, Hk, d, 16, rng, append=False, poison=True,
+                          shared=shared)
+    offs = np.array([0, 5, 7, 8, 11], dtype=np.int32)
+    pref = np.array([48, 64, 0, 37], dtype=np.int32)
+    out, lse = run_shared(batch, (offs, pref, 5, 64))
+    ref = oracle_step(batch)
+    assert_close(out, ref["out"], what=f"d={d} G={G}")
+    assert np.max(np.abs(lse - ref["lse"])) <= 1e-4
+
+
+def test_group_larger_than_a_chunk_and_block_size_32():
+    rng = np.random.default_rng(9)
+    G = 4  # 4 members per warp, 16 per CTA chunk
+    lens = list(rng.integers(200, 400, size=40))
+    batch = wl.make_batch("big", lens, 8 * G, 8, 128, 32, rng, append=True, poison=True,
+                          shared=[(list(range(40)), 6)])
+    out, _ = run_shared(batch, (np.array([0, 40], dtype=np.int32),
+                                np.array([192], dtype=np.int32), 40, 192))
+    ref = oracle_step(batch)
+    assert_close(out, ref["out"], what="40 members, bs 32")
+
+
+def test_matches_regular_entry_point():
+    batch = wl.workload(5, poison=False)
+    out, _ = run_shared(batch)
+    dev = to_dev(batch)
+    reg = pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                     dev["block_tables"], dev["context_lens"], batch.scale,
+                                     batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
+                                     batch.block_size, max_context_len=batch.max_context_len)
+    diff = np.abs(out.astype(np.float64) - reg.cpu().numpy().astype(np.float64))
+    assert diff.max() <= 2e-3
