@@ -341,6 +341,7 @@ int paged_decode_attention_prefix_shared(
     a.sh_acc = reinterpret_cast<float *>(base + sp.sh_acc);
     a.sh_m = reinterpret_cast<float *>(base + sp.sh_m);
     a.sh_l = reinterpret_cast<float *>(base + sp.sh_l);
+    a.defer_dep_wait = num_groups > 0 ? 1 : 0;  // the shared pass runs just before
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e = cudaSuccess;
     if (num_groups > 0) e = pkv::launch_decode_shared(a, stream);

@@ -141,7 +141,9 @@ __global__ void __launch_bounds__(kThreadsB)
     const int bs = a.block_size;
     char *ws = reinterpret_cast<char *>(a.ws_acc);
     int *counters = reinterpret_cast<int *>(ws);
-    grid_dependency_wait();  // the previous kernel in the stream (e.g. the append) is done
+    // the previous kernel in the stream (e.g. the append) is done; after the
+    // shared-prefix pass, only the reads of its partials have to wait
+    if (!a.defer_dep_wait) grid_dependency_wait();
 
     // --- tile prefix over sequences: contiguous chunk per thread, then a scan
     const int chunk = (B + kThreadsB - 1) / kThreadsB;
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kThreadsB)
     // ones get out = 0, lse = -inf; the others are the shared pass's result.
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         if (s_pre[b + 1] != s_pre[b]) continue;
+        grid_dependency_wait();  // the shared pass's partials are complete
         __half *ob = static_cast<__half *>(a.out) + static_cast<size_t>(b) * H * D;
         for (int i = tid; i < H * D; i += kThreadsB) {
             const int h = i / D;
@@ -303,6 +306,7 @@ __global__ void __launch_bounds__(kThreadsB)
         if (g >= G) return;
         const size_t bh = static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + g;
         if (s_skip[b] > 0) {  // fold in the shared-prefix partial states
+            grid_dependency_wait();  // complete and visible once the shared pass is done
             const size_t r0 = bh * a.sh_parts;
             float M = fm;
 #pragma unroll 4

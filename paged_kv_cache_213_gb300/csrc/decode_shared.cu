@@ -50,6 +50,9 @@ __global__ void __launch_bounds__(kWS * 32)
                          const __grid_constant__ CUtensorMap tmap_v) {
     using C = ShCfg<D>;
     constexpr int MPW = 16 / G;  // members per warp
+    // the suffix pass that follows may be scheduled as this grid's CTAs
+    // retire: it reads nothing this kernel writes until its own dependency wait
+    allow_dependent_launch();
     const int nwarps = blockDim.x >> 5;
     const int MPC = nwarps * MPW;  // members per CTA chunk
     const int nthreads = blockDim.x;

@@ -78,6 +78,11 @@ struct DecodeArgs {
     float *sh_acc;                // [B][H][sh_parts][D] shared-pass partial sums
     float *sh_m;                  // [B][H][sh_parts]
     float *sh_l;                  // [B][H][sh_parts]
+    // 1: the kernel before this one in the stream (the shared-prefix pass)
+    // writes only sh_acc / sh_m / sh_l, so the balanced kernel may run its
+    // prologue and private tiles before its grid-dependency wait and waits
+    // only before it reads those partials.  0: wait first.
+    int defer_dep_wait;
 };
 
 // Workspace carve-up shared by the planner and the launcher.
