@@ -20,6 +20,10 @@ What each function follows (page title, section):
     written into their assigned physical block slot.
   * ``partial`` / ``lse_merge`` -- the log-sum-exp split of the same softmax
     (FlashAttention-2, cited in section 14 of that page).
+  * ``e4m3_*``, ``append_f8``, ``decode_f8`` -- the FP8 KV cache that
+    "Roadmap: vLLM-style serving features for TornadoVM batched decode" (KV
+    cache list) names as future work; the format (OCP E4M3, per-tensor
+    scales, round-to-nearest-even with saturation) is this library's reading.
 """
 from __future__ import annotations
 
@@ -70,6 +74,21 @@ def _bind(lib):
     lib.pkvo_decode_partial.restype = c.c_int
     lib.pkvo_lse_merge.argtypes = [c.c_int, p, p, p, c.c_int, p, p]
     lib.pkvo_lse_merge.restype = None
+    lib.pkvo_e4m3_to_f64.argtypes = [c.c_uint8]
+    lib.pkvo_e4m3_to_f64.restype = c.c_double
+    lib.pkvo_f32_to_e4m3.argtypes = [c.c_float]
+    lib.pkvo_f32_to_e4m3.restype = c.c_uint8
+    lib.pkvo_quantize_e4m3_array.argtypes = [p, c.c_int64, c.c_float, p]
+    lib.pkvo_quantize_e4m3_array.restype = None
+    lib.pkvo_f32_to_e4m3_array.argtypes = [p, c.c_int64, p]
+    lib.pkvo_f32_to_e4m3_array.restype = None
+    lib.pkvo_append_f8.argtypes = [p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64,
+                                   c.c_float, c.c_float]
+    lib.pkvo_append_f8.restype = c.c_int
+    lib.pkvo_decode_f8.argtypes = [p, p, p, c.c_double, c.c_double, p, p, c.c_int, c.c_int,
+                                   c.c_int64, c.c_double, c.c_int, c.c_int, c.c_int, c.c_int, p,
+                                   p, p, c.c_int]
+    lib.pkvo_decode_f8.restype = c.c_int
     return lib
 
 
@@ -195,3 +214,87 @@ def lse_merge(m, l, acc, lib=None):
     lse = np.zeros(1)
     lib.pkvo_lse_merge(n, _ptr(m), _ptr(l), _ptr(acc), d, _ptr(out), _ptr(lse))
     return out, float(lse[0])
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# ---------------------------------------------------------------------------
+
+def e4m3_to_f64(code: int, lib=None) -> float:
+    """Value of one E4M3 code (NaN for 0x7f / 0xff)."""
+    return (lib or load()).pkvo_e4m3_to_f64(int(code))
+
+
+def e4m3_table(lib=None):
+    """Values of all 256 codes, float64 [256]."""
+    lib = lib or load()
+    return np.array([lib.pkvo_e4m3_to_f64(i) for i in range(256)])
+
+
+def f32_to_e4m3(y, lib=None):
+    """E4M3 codes (uint8) of fp32 values: nearest, ties to even, saturating."""
+    lib = lib or load()
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.zeros(y.shape, dtype=np.uint8)
+    lib.pkvo_f32_to_e4m3_array(_ptr(y), y.size, _ptr(out))
+    return out
+
+
+def quantize_e4m3(x16, scale, lib=None):
+    """Codes of fp16 values under a scale: E4M3(fp32(x) / fp32(scale))."""
+    lib = lib or load()
+    x = _u16(x16)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    lib.pkvo_quantize_e4m3_array(_ptr(x), x.size, float(np.float32(scale)), _ptr(out))
+    return out
+
+
+def _u8(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected uint8 codes, got {a.dtype}")
+    return a
+
+
+def append_f8(k_new, v_new, slot_mapping, k_cache8, v_cache8, block_size, k_scale, v_scale,
+              lib=None):
+    """Slot-mapped append into copies of FP8 caches ([NB, Hk, bs, d] uint8 codes)."""
+    lib = lib or load()
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    kc, vc = _u8(k_cache8).copy(), _u8(v_cache8).copy()
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T, Hk, d = k_new.shape
+    NB, Hk2, bs, d2 = kc.shape
+    if (Hk2, d2, bs) != (Hk, d, block_size) or v_new.shape != k_new.shape or vc.shape != kc.shape:
+        raise ValueError("shape mismatch")
+    rc = lib.pkvo_append_f8(_ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(kc), _ptr(vc), T, Hk,
+                            d, bs, NB, float(np.float32(k_scale)), float(np.float32(v_scale)))
+    if rc != 0:
+        raise OracleError("slot beyond the pool")
+    return kc, vc
+
+
+def decode_f8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, context_lens, scale,
+              n_q_heads, n_kv_heads, head_dim, block_size, mask=None, num_threads=0, lib=None):
+    """Paged decode attention over FP8 caches.  Returns (out f64 [B,H,d], lse f64 [B,H])."""
+    lib = lib or load()
+    q = _u16(q)
+    kc, vc = _u8(k_cache8), _u8(v_cache8)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, H, d = q.shape
+    NB = kc.shape[0]
+    if (H, d) != (n_q_heads, head_dim) or kc.shape != (NB, n_kv_heads, block_size, head_dim):
+        raise ValueError("shape mismatch")
+    if vc.shape != kc.shape or bt.shape[0] != B or cl.shape != (B,):
+        raise ValueError("shape mismatch")
+    out = np.full((B, H, d), np.nan)
+    lse = np.full((B, H), np.nan)
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8).reshape(B * H)
+    rc = lib.pkvo_decode_f8(_ptr(q), _ptr(kc), _ptr(vc), float(np.float32(k_scale)),
+                            float(np.float32(v_scale)), _ptr(bt), _ptr(cl), B, bt.shape[1], NB,
+                            float(scale), n_q_heads, n_kv_heads, head_dim, block_size, _ptr(m),
+                            _ptr(out), _ptr(lse), int(num_threads))
+    if rc != 0:
+        raise OracleError("invalid decode input")
+    return out, lse

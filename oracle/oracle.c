@@ -283,3 +283,196 @@ void pkvo_lse_merge(int n, const double *m, const double *l, const double *acc, 
     for (int k = 0; k < head_dim; ++k) out[k] /= denom;
     *lse = M + log(denom);
 }
+
+/* ---------------------------------------------------------------------------
+ * FP8 KV cache.  "Roadmap: vLLM-style serving features for TornadoVM batched
+ * decode", KV-cache list: a quantized (Q8/FP8) KV cache is named as future
+ * work, with no format or scaling rule.  Reading (listed in the design
+ * notes): OCP FP8 E4M3 ("e4m3fn": 1 sign, 4 exponent bits with bias 7, 3
+ * fraction bits, no infinities, S.1111.111 = NaN, largest finite 448), one
+ * scale per cache tensor supplied by the caller.  A cached value is
+ *     code = E4M3(y),  y = fp32(x) / fp32(scale)  (IEEE fp32 division),
+ * with E4M3() rounding to nearest, ties to even, and saturating finite
+ * overflow and infinities to +-448; a NaN gives the NaN code 0x7f.  The
+ * attended value is decode(code) * scale.
+ * ------------------------------------------------------------------------- */
+
+double pkvo_e4m3_to_f64(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int expo = (c >> 3) & 15;
+    int frac = c & 7;
+    double v;
+    if (expo == 15 && frac == 7) {
+        v = NAN;
+    } else if (expo == 0) {
+        v = ldexp((double)frac, -9);                /* zero or subnormal: frac * 2^-9 */
+    } else {
+        v = ldexp((double)(8 + frac), expo - 10);  /* (1.frac) * 2^(expo-7) */
+    }
+    return sign ? -v : v;
+}
+
+uint8_t pkvo_f32_to_e4m3(float y)
+{
+    uint8_t sign = signbit(y) ? 0x80 : 0;
+    if (isnan(y)) return 0x7f;
+    double a = fabs((double)y);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);   /* saturate (also +-inf) */
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: value = m * 2^-9, m in [0, 8]; m == 8 is the
+         * smallest normal number, whose bit pattern is 0x08 */
+        double m = rint(ldexp(a, 9));
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int e2;
+    frexp(a, &e2);
+    int e = e2 - 1;                     /* a in [2^e, 2^(e+1)), e in [-6, 8] */
+    double m = rint(ldexp(a, 3 - e));   /* 4-bit significand, in [8, 16] */
+    if (m == 16.0) { m = 8.0; e += 1; }
+    if (e > 8 || (e == 8 && m > 14.0)) return (uint8_t)(sign | 0x7e);
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((int)m - 8));
+}
+
+static double g_e4m3[256];
+static int g_e4m3_ready = 0;
+
+static void e4m3_table_init(void)
+{
+    if (g_e4m3_ready) return;
+    for (int i = 0; i < 256; ++i) g_e4m3[i] = pkvo_e4m3_to_f64((uint8_t)i);
+    g_e4m3_ready = 1;
+}
+
+/* The code of one fp16 input under a scale: the fp16 value is exact in fp32,
+ * the quotient is one correctly rounded fp32 division. */
+uint8_t pkvo_quantize_e4m3(uint16_t x_f16, float scale)
+{
+    f16_table_init();
+    volatile float x = (float)g_f16[x_f16];
+    volatile float y = x / scale;
+    return pkvo_f32_to_e4m3(y);
+}
+
+/* Slot-mapped append into FP8 caches (same slot rule as pkvo_append). */
+int pkvo_append_f8(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slot_mapping,
+                   uint8_t *k_cache, uint8_t *v_cache, int num_tokens, int n_kv_heads,
+                   int head_dim, int block_size, int64_t num_blocks, float k_scale,
+                   float v_scale)
+{
+    int rc = 0;
+    for (int i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * (int64_t)block_size) { rc = -1; continue; }
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int j = 0; j < n_kv_heads; ++j) {
+            const uint16_t *ksrc = k_new + ((int64_t)i * n_kv_heads + j) * head_dim;
+            const uint16_t *vsrc = v_new + ((int64_t)i * n_kv_heads + j) * head_dim;
+            int64_t row = ((block * n_kv_heads + j) * block_size + offset) * head_dim;
+            for (int k = 0; k < head_dim; ++k) {
+                k_cache[row + k] = pkvo_quantize_e4m3(ksrc[k], k_scale);
+                v_cache[row + k] = pkvo_quantize_e4m3(vsrc[k], v_scale);
+            }
+        }
+    }
+    return rc;
+}
+
+/* attend_range over FP8 caches: K_t = decode(code) * k_scale and
+ * V_t = decode(code) * v_scale, gathered the same way. */
+static int attend_range_f8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                           double k_scale, double v_scale, const int32_t *block_tables,
+                           int max_blocks_per_seq, int64_t num_blocks, double scale,
+                           int n_q_heads, int n_kv_heads, int head_dim, int block_size, int b,
+                           int h, int t_begin, int t_end, double *m_out, double *l_out,
+                           double *acc)
+{
+    int group = n_q_heads / n_kv_heads;
+    int j = h / group;
+    int n = t_end - t_begin;
+    for (int k = 0; k < head_dim; ++k) acc[k] = 0.0;
+    *m_out = -INFINITY;
+    *l_out = 0.0;
+    if (n <= 0) return 0;
+    const uint16_t *qv = q + ((int64_t)b * n_q_heads + h) * head_dim;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!s) return -2;
+    for (int t = t_begin; t < t_end; ++t) {
+        int32_t block = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+        if (block < 0 || block >= num_blocks) { free(s); return -1; }
+        const uint8_t *kt = k_cache + (((int64_t)block * n_kv_heads + j) * block_size +
+                                       t % block_size) * head_dim;
+        double dot = 0.0;
+        for (int k = 0; k < head_dim; ++k) dot += g_f16[qv[k]] * (g_e4m3[kt[k]] * k_scale);
+        s[t - t_begin] = scale * dot;
+    }
+    double m = -INFINITY;
+    for (int i = 0; i < n; ++i) if (s[i] > m) m = s[i];
+    double l = 0.0;
+    for (int i = 0; i < n; ++i) { s[i] = exp(s[i] - m); l += s[i]; }
+    for (int t = t_begin; t < t_end; ++t) {
+        int32_t block = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+        const uint8_t *vt = v_cache + (((int64_t)block * n_kv_heads + j) * block_size +
+                                       t % block_size) * head_dim;
+        double p = s[t - t_begin];
+        for (int k = 0; k < head_dim; ++k) acc[k] += p * (g_e4m3[vt[k]] * v_scale);
+    }
+    free(s);
+    *m_out = m;
+    *l_out = l;
+    return 0;
+}
+
+/* pkvo_decode over FP8 caches. */
+int pkvo_decode_f8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                   double k_scale, double v_scale, const int32_t *block_tables,
+                   const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                   int64_t num_blocks, double scale, int n_q_heads, int n_kv_heads,
+                   int head_dim, int block_size, const uint8_t *mask, double *out, double *lse,
+                   int num_threads)
+{
+    f16_table_init();
+    e4m3_table_init();
+    if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -1;
+    for (int b = 0; b < num_seqs; ++b) {
+        int L = context_lens[b];
+        if (L < 0 || L > max_blocks_per_seq * block_size) return -1;
+    }
+    int failed = 0;
+    int64_t pairs = (int64_t)num_seqs * n_q_heads;
+#ifdef _OPENMP
+    int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt) reduction(| : failed)
+#endif
+    for (int64_t bh = 0; bh < pairs; ++bh) {
+        if (mask && !mask[bh]) continue;
+        int b = (int)(bh / n_q_heads);
+        int h = (int)(bh % n_q_heads);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        double m, l;
+        int rc = attend_range_f8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                 max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
+                                 head_dim, block_size, b, h, 0, context_lens[b], &m, &l, acc);
+        if (rc != 0) { failed = 1; free(acc); continue; }
+        for (int k = 0; k < head_dim; ++k)
+            if (out) out[bh * head_dim + k] = (l > 0.0) ? acc[k] / l : 0.0;
+        if (lse) lse[bh] = (l > 0.0) ? m + log(l) : -INFINITY;
+        free(acc);
+    }
+    (void)num_threads;
+    return failed ? -1 : 0;
+}
+
+/* pkvo_quantize_e4m3 over an array (n codes). */
+void pkvo_quantize_e4m3_array(const uint16_t *x_f16, int64_t n, float scale, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; ++i) codes[i] = pkvo_quantize_e4m3(x_f16[i], scale);
+}
+
+/* pkvo_f32_to_e4m3 over an array of fp32 values. */
+void pkvo_f32_to_e4m3_array(const float *y, int64_t n, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; ++i) codes[i] = pkvo_f32_to_e4m3(y[i]);
+}

@@ -402,6 +402,161 @@ def pin_rejects_bad_input(lib, seed=18):
         raise AssertionError(f"bad {bad} accepted")
 
 
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) KV cache pins: torch's float8_e4m3fn conversions are the
+# independent library routine (they round to nearest-even but turn overflow
+# into NaN, so the saturation of the library's reading is pinned by closed
+# forms instead)
+# ----------------------------------------------------------------------------
+
+def _torch_e4m3_codes(y32):
+    """torch's E4M3 codes of fp32 values already inside [-448, 448]."""
+    t = torch.from_numpy(np.ascontiguousarray(y32, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_e4m3_values(codes):
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_decode(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = _torch_e4m3_values(codes)
+    got = np.array([lib.pkvo_e4m3_to_f64(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def pin_e4m3_encode(lib, seed=21):
+    rng = np.random.default_rng(seed)
+    codes = np.arange(256, dtype=np.uint8)
+    vals = _torch_e4m3_values(codes)
+    finite = ~np.isnan(vals)
+    # every code round-trips (both zeros included)
+    back = oracle.f32_to_e4m3(vals[finite].astype(np.float32), lib=lib)
+    assert np.array_equal(back, codes[finite])
+    # midpoints between neighbours, and random values, against torch (in range)
+    pos = np.sort(np.unique(np.abs(vals[finite])))
+    mids = (pos[:-1] + pos[1:]) / 2.0
+    ys = np.concatenate([mids, -mids, rng.uniform(-447.0, 447.0, 20000),
+                         rng.standard_normal(20000) * 10.0 ** rng.integers(-4, 2, 20000)])
+    ys = ys.astype(np.float32)
+    ys = ys[np.abs(ys) < 448.0]
+    got = oracle.f32_to_e4m3(ys, lib=lib)
+    ref = _torch_e4m3_codes(ys)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(ys[i]), hex(got[i]), hex(ref[i])) for i in bad[:5]]
+    # closed forms of the saturating reading: finite overflow and infinities
+    # go to +-448, NaN to the NaN code
+    sat = np.array([448.0, 455.0, 463.9, 464.0, 480.0, 1e30, np.inf], dtype=np.float32)
+    assert np.all(oracle.f32_to_e4m3(sat, lib=lib) == 0x7E)
+    assert np.all(oracle.f32_to_e4m3(-sat, lib=lib) == 0xFE)
+    assert oracle.f32_to_e4m3(np.array([np.nan], dtype=np.float32), lib=lib)[0] == 0x7F
+    tiny = np.array([2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -9, 2.0 ** -11], dtype=np.float32)
+    assert list(oracle.f32_to_e4m3(tiny, lib=lib)) == [0x00, 0x02, 0x01, 0x00]
+
+
+def pin_e4m3_quantize(lib):
+    """Every finite fp16 value under several scales: E4M3(fp32(x) / fp32(s)),
+    the quotient by numpy's IEEE fp32 division, the rounding by torch."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x16 = bits.view(np.float16)
+    ok = np.isfinite(x16)
+    bits, x16 = bits[ok], x16[ok]
+    for s in (1.0, 0.0123, 3.5, 1.0 / 64, 448.0 / 65504.0):
+        s32 = np.float32(s)
+        y = x16.astype(np.float32) / s32
+        got = oracle.quantize_e4m3(bits, s32, lib=lib)
+        inr = np.abs(y) < 448.0
+        ref = np.where(y >= 0, 0x7E, 0xFE).astype(np.uint8)
+        ref[inr] = _torch_e4m3_codes(y[inr])
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, (s, [(float(x16[i]), hex(got[i]), hex(ref[i])) for i in bad[:5]])
+    inf = np.array([0x7C00, 0xFC00], dtype=np.uint16)
+    assert list(oracle.quantize_e4m3(inf, 1.0, lib=lib)) == [0x7E, 0xFE]
+
+
+def _paginate_codes(K8, V8, lens, bs, rng, poison=True):
+    """paginate() for uint8 code arrays (poison: the NaN code 0x7f)."""
+    kc16, vc16, bt = paginate(K8.astype(np.float16), V8.astype(np.float16), lens, bs, rng,
+                              poison=poison)
+    # codes 0..255 are exact in fp16 and NaN marks the poisoned rows
+    kc = np.where(np.isnan(kc16), 0x7F, kc16).astype(np.uint8)
+    vc = np.where(np.isnan(vc16), 0x7F, vc16).astype(np.uint8)
+    return kc, vc, bt
+
+
+def pin_f8_dense(lib, seed=22):
+    """FP8 paged attention = float64 SDPA over torch-dequantized K/V."""
+    rng = np.random.default_rng(seed)
+    for (B, H, Hk, d, bs, lens, ks, vs) in [(3, 4, 2, 64, 16, (1, 17, 40), 0.02, 0.015),
+                                            (2, 8, 1, 128, 16, (33, 16), 1.0, 0.5),
+                                            (2, 8, 2, 64, 8, (15, 64), 0.003, 2.0)]:
+        q = randn16(rng, (B, H, d))
+        Lmax = max(lens)
+        K8 = rng.integers(0, 256, (B, Hk, Lmax, d)).astype(np.uint8)
+        V8 = rng.integers(0, 256, (B, Hk, Lmax, d)).astype(np.uint8)
+        K8[(K8 & 0x7F) == 0x7F] = 0x3C   # no NaN codes in attended rows
+        V8[(V8 & 0x7F) == 0x7F] = 0x41
+        kc, vc, bt = _paginate_codes(K8, V8, lens, bs, rng)
+        scale = 1.0 / math.sqrt(d)
+        out, lse = oracle.decode_f8(q, kc, vc, ks, vs, bt, np.asarray(lens, np.int32), scale,
+                                    H, Hk, d, bs, lib=lib)
+        Kd = _torch_e4m3_values(K8) * float(np.float32(ks))
+        Vd = _torch_e4m3_values(V8) * float(np.float32(vs))
+        ref, ref_lse = dense_reference(q, Kd, Vd, lens, scale, H, Hk)
+        assert np.max(np.abs(out - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+        assert np.max(np.abs(lse - ref_lse)) <= 1e-12 * max(1.0, np.max(np.abs(ref_lse)))
+
+
+def pin_f8_append(lib, seed=23):
+    """FP8 append = torch quantization (clamped to +-448 first) scattered by
+    numpy fancy indexing; -1 slots skipped; other bytes untouched."""
+    rng = np.random.default_rng(seed)
+    NB, Hk, bs, d = 7, 2, 16, 64
+    kc = rng.integers(0, 256, (NB, Hk, bs, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, (NB, Hk, bs, d)).astype(np.uint8)
+    T = 12
+    slots = rng.choice(NB * bs, size=T, replace=False).astype(np.int64)
+    slots[[3, 7]] = -1
+    kn = (rng.standard_normal((T, Hk, d)) * 40.0).astype(np.float16)
+    vn = randn16(rng, (T, Hk, d))
+    ks, vs = np.float32(0.05), np.float32(0.011)
+    k2, v2 = oracle.append_f8(kn, vn, slots, kc, vc, bs, ks, vs, lib=lib)
+    keep = slots >= 0
+    for cache, new, s, got in ((kc, kn, ks, k2), (vc, vn, vs, v2)):
+        y = np.clip(new.astype(np.float32) / s, -448.0, 448.0)
+        codes = _torch_e4m3_codes(y)
+        ref = cache.copy()
+        flat = ref.transpose(0, 2, 1, 3).reshape(NB * bs, Hk, d).copy()
+        flat[slots[keep]] = codes[keep]
+        ref = flat.reshape(NB, bs, Hk, d).transpose(0, 2, 1, 3)
+        assert np.array_equal(got, np.ascontiguousarray(ref))
+    assert np.any(np.abs(kn.astype(np.float32) / ks) > 448.0)  # saturation exercised
+
+
+def pin_f8_poison(lib, seed=24):
+    """NaN codes in unread rows, blocks and table entries change no output bit."""
+    rng = np.random.default_rng(seed)
+    B, H, Hk, d, bs, lens = 3, 4, 2, 64, 16, (17, 32, 5)
+    q = randn16(rng, (B, H, d))
+    K8 = rng.integers(0, 0x70, (B, Hk, max(lens), d)).astype(np.uint8)
+    V8 = rng.integers(0x80, 0xF0, (B, Hk, max(lens), d)).astype(np.uint8)
+    kc, vc, bt = _paginate_codes(K8, V8, lens, bs, np.random.default_rng(1), poison=False)
+    kc2, vc2, bt2 = _paginate_codes(K8, V8, lens, bs, np.random.default_rng(1), poison=True)
+    assert np.any(kc2 == 0x7F)
+    a = oracle.decode_f8(q, kc, vc, 0.1, 0.2, bt, np.asarray(lens, np.int32), 0.125, H, Hk, d,
+                         bs, lib=lib)
+    b = oracle.decode_f8(q, kc2, vc2, 0.1, 0.2, bt2, np.asarray(lens, np.int32), 0.125, H, Hk,
+                         d, bs, lib=lib)
+    assert np.all(np.isfinite(a[0])) and np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 ALL_PINS = [pin_fp16_decode, pin_fp16_encode, pin_dense_sdpa, pin_closed_forms,
             pin_invariances, pin_merge, pin_poison, pin_append, pin_append_then_attend,
-            pin_rejects_bad_input]
+            pin_rejects_bad_input, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_quantize,
+            pin_f8_dense, pin_f8_append, pin_f8_poison]

@@ -36,6 +36,14 @@ MUTANTS = [
     ("encode_truncates", "double m = rint(ldexp(a, 10 - e));", "double m = floor(ldexp(a, 10 - e));"),
     ("append_offset", "int64_t offset = slot % block_size;", "int64_t offset = 0;"),
     ("append_keeps_negative", "if (slot < 0) continue;", "if (slot < -1) continue;"),
+    ("e4m3_bias", "ldexp((double)(8 + frac), expo - 10)", "ldexp((double)(8 + frac), expo - 9)"),
+    ("e4m3_truncates", "double m = rint(ldexp(a, 3 - e));", "double m = floor(ldexp(a, 3 - e));"),
+    ("e4m3_no_saturation", "if (a >= 448.0) return (uint8_t)(sign | 0x7e);",
+     "if (a >= 464.0) return 0x7f;"),
+    ("e4m3_subnormal", "double m = rint(ldexp(a, 9));", "double m = rint(ldexp(a, 8));"),
+    ("f8_quantize_multiplies", "volatile float y = x / scale;", "volatile float y = x * scale;"),
+    ("f8_k_scale_dropped", "(g_e4m3[kt[k]] * k_scale)", "g_e4m3[kt[k]]"),
+    ("f8_v_scale_dropped", "acc[k] += p * (g_e4m3[vt[k]] * v_scale);", "acc[k] += p * g_e4m3[vt[k]];"),
     ("empty_range_bound", "for (int t = t_begin; t < t_end; ++t) {\n        const uint16_t *kt",
      "for (int t = t_begin; t < t_end - (t_end - t_begin > 1); ++t) {\n        const uint16_t *kt"),
 ]
@@ -61,7 +69,7 @@ lib.pkvo_init()
 for pin in pins.ALL_PINS:
     try:
         pin(lib)
-    except (AssertionError, oracle.OracleError, ValueError, FloatingPointError) as e:
+    except (AssertionError, oracle.OracleError, ValueError, FloatingPointError, TypeError) as e:
         print("caught by", pin.__name__)
         sys.exit(3)
 sys.exit(0)
