@@ -213,6 +213,46 @@ int paged_decode_attention_prefix_shared(
     void *cuda_stream);
 
 /*
+ * FP8 KV cache.  "Roadmap: vLLM-style serving features for TornadoVM batched
+ * decode", KV-cache list, names a quantized (Q8/FP8) KV cache as future work
+ * and fixes no format; this library's reading:
+ *  - k_cache, v_cache hold one byte per value: OCP FP8 E4M3 codes ("e4m3fn":
+ *    1 sign, 4 exponent bits with bias 7, 3 fraction bits, no infinities,
+ *    S.1111.111 is NaN, largest finite 448), same [num_blocks][n_kv_heads]
+ *    [block_size][head_dim] layout as the fp16 caches (a 16 x 128 tile is
+ *    2 KiB);
+ *  - one scale per cache tensor (k_scale, v_scale; finite, > 0), chosen by
+ *    the caller, e.g. max |value| / 448;
+ *  - paged_kv_append_fp8 stores code = E4M3(fp32(x) / k_scale) for each fp16
+ *    value x of k_new (v_scale for v_new): one correctly rounded fp32
+ *    division, then round to nearest, ties to even, with finite overflow and
+ *    infinities saturated to +-448 (a NaN stores a NaN code);
+ *  - paged_decode_attention_fp8 attends over the values code * k_scale and
+ *    code * v_scale, with the same results as paged_decode_attention
+ *    otherwise (fp32 accumulation, fp16 out, lse).
+ * Requirements: head_dim % 16 == 0 for the append; the attention runs on the
+ * balanced split only (head_dim 64 or 128, n_q/n_kv in {1, 2, 4, 8},
+ * block_size a multiple of 16, at most 2048 sequences; PKV_ERR_UNSUPPORTED
+ * otherwise).  paged_decode_plan_fp8 gives its workspace bytes; the
+ * workspace must be zero-filled before its first use, as for the fp16 call.
+ * Pointers, errors and ownership as for the fp16 calls.
+ */
+int paged_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                        void *k_cache, void *v_cache, int num_tokens, int n_kv_heads,
+                        int head_dim, int block_size, int64_t num_blocks, float k_scale,
+                        float v_scale, int32_t *err_word, void *cuda_stream);
+int paged_decode_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                          int block_size, int max_blocks_per_seq, int max_context_len,
+                          size_t *workspace_bytes_out);
+int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                               int64_t num_blocks, float scale, float k_scale, float v_scale,
+                               int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                               int max_context_len, void *workspace, size_t workspace_bytes,
+                               float *lse_out, int32_t *err_word, void *cuda_stream);
+
+/*
  * Allocation-free variant of paged_decode_attention.  The pages have no
  * counterpart to this call.  It serves callers that cannot allocate device
  * memory and so cannot supply the split-K workspace: an operator running

@@ -13,13 +13,16 @@ from .binding import (  # noqa: F401
     PKV_ERRBIT_TIMEOUT,
     PagedKVError,
     decode_plan,
+    decode_plan_fp8,
     default_scale,
     get_error,
     library,
     library_path,
     paged_decode_attention,
+    paged_decode_attention_fp8,
     paged_decode_attention_prefix_shared,
     paged_kv_append,
+    paged_kv_append_fp8,
     prefix_shared_plan,
     status_string,
 )

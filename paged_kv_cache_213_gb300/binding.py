@@ -327,3 +327,109 @@ def paged_decode_attention_prefix_shared(q, k_cache, v_cache, block_tables, cont
                 _ptr(lse), _ptr(err_word), _stream_handle(dev))
     _check("paged_decode_attention_prefix_shared", rc)
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV caches: uint8 tensors of codes, one scale per cache tensor
+# ---------------------------------------------------------------------------
+
+def paged_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                        err_word=None):
+    """Quantize k_new/v_new [T, Hk, d] (fp16) to E4M3 codes (x / scale, nearest-even,
+    saturating) into slots of k_cache/v_cache [NB, Hk, bs, d] (uint8), in place."""
+    lib = library()
+    fn = lib.paged_kv_append_fp8
+    c = ctypes
+    p = c.c_void_p
+    fn.argtypes = [p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_float,
+                   c.c_float, p, p]
+    fn.restype = c.c_int
+    dev = k_cache.device
+    _need(k_new, "k_new", torch.float16, dev)
+    _need(v_new, "v_new", torch.float16, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    _need(k_cache, "k_cache", torch.uint8, dev)
+    _need(v_cache, "v_cache", torch.uint8, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must both be [num_blocks, n_kv_heads, block_size, head_dim]")
+    NB, Hk, bs, d = k_cache.shape
+    if k_new.dim() != 3 or k_new.shape[1:] != (Hk, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens, n_kv_heads, head_dim]")
+    T = k_new.shape[0]
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), T,
+                Hk, d, bs, NB, float(k_scale), float(v_scale), _ptr(err_word),
+                _stream_handle(dev))
+    _check("paged_kv_append_fp8", rc)
+
+
+def decode_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                    max_context_len=0):
+    """Workspace bytes of paged_decode_attention_fp8."""
+    lib = library()
+    fn = lib.paged_decode_plan_fp8
+    c = ctypes
+    fn.argtypes = [c.c_int] * 7 + [c.POINTER(c.c_size_t)]
+    fn.restype = c.c_int
+    W = c.c_size_t(0)
+    _check("paged_decode_plan_fp8",
+           fn(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+              max_context_len, c.byref(W)))
+    return W.value
+
+
+def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
+                               v_scale, n_q_heads, n_kv_heads, head_dim, block_size,
+                               max_context_len=None, out=None, workspace=None, lse=None,
+                               err_word=None):
+    """Decode attention over E4M3 caches [NB, Hk, bs, d] (uint8): keys and values are
+    code * k_scale and code * v_scale.  Returns out [B, H, d] fp16."""
+    lib = library()
+    fn = lib.paged_decode_attention_fp8
+    c = ctypes
+    p = c.c_void_p
+    fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float, c.c_float,
+                   c.c_float, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p,
+                   p]
+    fn.restype = c.c_int
+    dev = q.device
+    _need(q, "q", torch.float16, dev)
+    _need(k_cache, "k_cache", torch.uint8, dev)
+    _need(v_cache, "v_cache", torch.uint8, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    B = q.shape[0]
+    if q.dim() != 3 or q.shape[1:] != (n_q_heads, head_dim):
+        raise ValueError("q must be [num_seqs, n_q_heads, head_dim]")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or \
+            k_cache.shape[1:] != (n_kv_heads, block_size, head_dim):
+        raise ValueError("caches must be [num_blocks, n_kv_heads, block_size, head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, MB], context_lens [B]")
+    MB = block_tables.shape[1]
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    ws = decode_plan_fp8(B, n_q_heads, n_kv_heads, head_dim, block_size, MB, mcl)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, dev)
+    if workspace is None:
+        # zero-filled: the balanced split keeps arrival counters in it
+        workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), float(k_scale),
+                float(v_scale), n_q_heads, n_kv_heads, head_dim, block_size, mcl,
+                _ptr(workspace), workspace.numel(), _ptr(lse), _ptr(err_word),
+                _stream_handle(dev))
+    _check("paged_decode_attention_fp8", rc)
+    return out

@@ -212,6 +212,119 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) KV caches
+// ---------------------------------------------------------------------------
+
+int paged_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                        void *k_cache, void *v_cache, int num_tokens, int n_kv_heads,
+                        int head_dim, int block_size, int64_t num_blocks, float k_scale,
+                        float v_scale, int32_t *err_word, void *cuda_stream) {
+    if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || head_dim % 16 != 0 ||
+        num_blocks <= 0 || block_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
+        !(v_scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8) || (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    pkv::AppendArgs a{k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens,
+                      n_kv_heads, head_dim, block_size, num_blocks, err_word};
+    const cudaError_t e =
+        pkv::launch_append_f8(a, k_scale, v_scale, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The balanced plan for E4M3 caches (its own occupancy, hence grid and workspace).
+int make_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                  int max_blocks_per_seq, int max_context_len, Plan *plan) {
+    int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                       max_context_len, 0, plan);
+    if (rc != PKV_OK) return rc;
+    if (!plan->balanced) return PKV_ERR_UNSUPPORTED;  // E4M3 runs on the balanced kernel only
+    if (!pkv::balanced_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, plan->max_len, &plan->bal,
+                            true))
+        return PKV_ERR_CUDA;
+    plan->ws_bytes = plan->bal.ws_bytes;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_decode_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                          int block_size, int max_blocks_per_seq, int max_context_len,
+                          size_t *workspace_bytes_out) {
+    Plan plan{};
+    const int rc = make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                 max_blocks_per_seq, max_context_len, &plan);
+    if (rc == PKV_OK && workspace_bytes_out) *workspace_bytes_out = plan.ws_bytes;
+    return rc;
+}
+
+int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                               int64_t num_blocks, float scale, float k_scale, float v_scale,
+                               int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                               int max_context_len, void *workspace, size_t workspace_bytes,
+                               float *lse_out, int32_t *err_word, void *cuda_stream) {
+    if (num_blocks <= 0 || !std::isfinite(scale) || !std::isfinite(k_scale) ||
+        !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    Plan plan{};
+    int rc = make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, max_context_len, &plan);
+    if (rc != PKV_OK) return rc;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+        (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
+        return PKV_ERR_UNSUPPORTED;  // row indices are 32-bit
+    pkv::DecodeArgs a{};
+    a.ws_acc = static_cast<float *>(workspace);
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.lse_out = lse_out;
+    a.err = err_word;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    // the logits of E4M3 keys: q . (code * k_scale) * scale
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * k_scale * 1.4426950408889634);
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.max_context_len = plan.max_len;
+    a.partition_tokens = 0;
+    a.max_parts = 1;
+    a.kv_fp8 = 1;
+    a.v_scale = v_scale;
+    const cudaError_t e =
+        pkv::launch_decode_balanced(a, plan.bal, static_cast<cudaStream_t>(cuda_stream));
+    if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace {

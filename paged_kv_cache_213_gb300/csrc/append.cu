@@ -7,6 +7,7 @@
 // One thread moves one 16-byte vector of K and one of V: coalesced along
 // head_dim, bit-exact.
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "pagedkv.h"
 #include "pkv_internal.h"
@@ -100,6 +101,79 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
     copy_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src, dst, tokens,
         num_copies, n_kv_heads, chunks, block_size, num_blocks, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv
+
+// FP8 KV cache append (the quantized KV cache the "Roadmap: vLLM-style
+// serving features for TornadoVM batched decode" page lists as future work;
+// E4M3 with one scale per cache tensor is this library's reading): each
+// value is stored as E4M3(x / scale), the quotient one correctly rounded
+// fp32 division, the conversion round-to-nearest-even with finite overflow
+// saturated to +-448 (the hardware cvt.rn.satfinite).  One thread turns 16
+// fp16 values of K and of V (two 16-byte loads each) into one 16-byte store.
+namespace pkv {
+namespace {
+
+__device__ __forceinline__ uint4 quantize16(const uint4 &lo, const uint4 &hi, float scale) {
+    const __half2 *h0 = reinterpret_cast<const __half2 *>(&lo);
+    const __half2 *h1 = reinterpret_cast<const __half2 *>(&hi);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 a = i < 2 ? h0[2 * i] : h1[2 * i - 4];
+        const __half2 b = i < 2 ? h0[2 * i + 1] : h1[2 * i - 3];
+        const float2 fa = __half22float2(a);
+        const float2 fb = __half22float2(b);
+        const __nv_fp8x2_storage_t ca = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(fa.x, scale), __fdiv_rn(fa.y, scale)), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t cb = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(fb.x, scale), __fdiv_rn(fb.y, scale)), __NV_SATFINITE, __NV_E4M3);
+        w[i] = static_cast<uint32_t>(ca) | (static_cast<uint32_t>(cb) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(256)
+    append_f8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                     const int64_t *__restrict__ slots, uint4 *__restrict__ k_cache,
+                     uint4 *__restrict__ v_cache, long long total, int n_kv_heads, int chunks,
+                     int block_size, long long num_slots, float k_scale, float v_scale,
+                     int32_t *err) {
+    allow_dependent_launch();  // the attention kernel may get scheduled meanwhile
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int c = static_cast<int>(idx % chunks);  // 16-value chunk of the row
+    const long long r = idx / chunks;
+    const int j = static_cast<int>(r % n_kv_heads);
+    const long long i = r / n_kv_heads;
+    const long long s = slots[i];
+    if (s < 0) return;  // padding token
+    if (s >= num_slots) {
+        if (c == 0 && j == 0) flag_error(err, PKV_ERRBIT_SLOT);
+        return;
+    }
+    const long long block = s / block_size;
+    const long long row = s % block_size;
+    const long long dst = ((block * n_kv_heads + j) * block_size + row) * chunks + c;
+    k_cache[dst] = quantize16(k_new[2 * idx], k_new[2 * idx + 1], k_scale);
+    v_cache[dst] = quantize16(v_new[2 * idx], v_new[2 * idx + 1], v_scale);
+}
+
+}  // namespace
+
+cudaError_t launch_append_f8(const AppendArgs &a, float k_scale, float v_scale,
+                             cudaStream_t stream) {
+    const int chunks = a.head_dim / 16;
+    const long long total = static_cast<long long>(a.num_tokens) * a.n_kv_heads * chunks;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    append_f8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(a.k_new), static_cast<const uint4 *>(a.v_new), a.slot_mapping,
+        static_cast<uint4 *>(a.k_cache), static_cast<uint4 *>(a.v_cache), total, a.n_kv_heads,
+        chunks, a.block_size, a.num_blocks * a.block_size, k_scale, v_scale, a.err);
     return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@
 // partial results from FlashAttention-2 (section 14 references).
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -48,13 +49,48 @@ constexpr int kMaxWorkers = 16384;  // size of the counter region
 constexpr int kMinUnits = 4;        // fewest units a working warp takes
 constexpr float kLn2b = 0.69314718055994531f;
 
-template <int D, int G>
+template <int D, int G, bool F8>
 struct BalCfg : MmaCfg<D> {
-    static constexpr int Q_BYTES = G * D * 2;                      // the group's query rows
-    static constexpr int SLOT_BYTES = 2 * MmaCfg<D>::TILE_BYTES;   // K tile, V tile
-    static constexpr int PIPE_BYTES = kW * kS * SLOT_BYTES;
+    static constexpr int Q_BYTES = G * D * 2;  // the group's query rows
+    // one tile of one cache in the ring: fp16 (TMA boxes) or E4M3 bytes
+    static constexpr int KV_BYTES = F8 ? kMmaTile * D : MmaCfg<D>::TILE_BYTES;
+    static constexpr int SLOT_BYTES = 2 * KV_BYTES;  // K tile, V tile
+    // FP8: the converted fp16 K and V tiles the tile math reads
+    static constexpr int STAGE_BYTES = F8 ? 2 * MmaCfg<D>::TILE_BYTES : 0;
+    static constexpr int WARP_BYTES = kS * SLOT_BYTES + STAGE_BYTES;  // multiple of 1024
+    static constexpr int PIPE_BYTES = kW * WARP_BYTES;
     static constexpr int QS_BYTES = kW * kS * Q_BYTES;
 };
+
+// E4M3 tile (16 rows x D bytes, row-major) -> the fp16 tile layout that the
+// TMA loads give (D/64 boxes of 16 rows x 128 bytes, 128-byte swizzle).
+// Every code is exact in fp16 (cvt.rn.f16x2.e4m3x2); lane-contiguous reads.
+template <int D>
+__device__ __forceinline__ void e4m3_tile_to_f16(const unsigned char *src, unsigned char *dst,
+                                                 int lane) {
+    constexpr int ROW_UNITS = D / 16;  // 16-byte units of an E4M3 row
+#pragma unroll
+    for (int u = lane; u < kMmaTile * ROW_UNITS; u += 32) {
+        const int row = u / ROW_UNITS;
+        const int col = (u % ROW_UNITS) * 16;  // first of the unit's 16 columns
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + u * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(w[i] & 0xffffu), __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+            h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+            h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+        }
+        unsigned char *box = dst + (col / 64) * MmaCfg<D>::BOX_BYTES;
+        const int unit = (col % 64) / 8;
+        *reinterpret_cast<uint4 *>(box + swz(row, unit)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(box + swz(row, unit + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
 
 // Workspace: int counters[kMaxWorkers] at offset 0 (whatever the plan, so
 // that a workspace reused by another plan still starts zeroed), then one
@@ -112,12 +148,12 @@ __device__ __forceinline__ void advance(Cursor &c, const int *pre, int B) {
     while (c.b < B && pre[c.b + 1] == pre[c.b]) ++c.b;
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kThreadsB)
     decode_balanced_kernel(const __grid_constant__ DecodeArgs a,
                            const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const int workers) {
-    using C = BalCfg<D, G>;
+    using C = BalCfg<D, G, F8>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kW][kS];
     __shared__ uint64_t merge_bar[kW];
@@ -177,8 +213,10 @@ __global__ void __launch_bounds__(kThreadsB)
     }
     if (lane == 31) s_scan[warp] = incl;
     if (tid == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
+        if constexpr (!F8) {  // E4M3 tiles use plain bulk copies, no tensor map
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
         for (int w = 0; w < kW; ++w) {
             for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
             mbar_init(&merge_bar[w], 1);
@@ -231,7 +269,8 @@ __global__ void __launch_bounds__(kThreadsB)
     const int n = min(T, w0 + U) - w0;
     if (n <= 0) return;  // no CTA-wide barriers below
 
-    unsigned char *my_pipe = smem + warp * kS * C::SLOT_BYTES;
+    unsigned char *my_pipe = smem + warp * C::WARP_BYTES;
+    unsigned char *my_stage = my_pipe + kS * C::SLOT_BYTES;  // FP8: converted tiles
     unsigned char *my_q = qslots + warp * kS * C::Q_BYTES;
     Cursor pc = locate(w0, s_pre, B);  // producer cursor
     Cursor cc = pc;                        // consumer cursor
@@ -267,16 +306,24 @@ __global__ void __launch_bounds__(kThreadsB)
             const bool ok = id >= 0 && id < a.num_blocks;
             if (!ok) flag_error(a.err, PKV_ERRBIT_BLOCK_ID);
             s_ok[warp][slot] = ok;
-            const uint32_t bytes = (ok ? 2 * C::TILE_BYTES : 0) + (newseg ? C::Q_BYTES : 0);
+            const uint32_t bytes = (ok ? 2 * C::KV_BYTES : 0) + (newseg ? C::Q_BYTES : 0);
             mbar_arrive_expect_tx(bar, bytes);
             if (ok) {
                 unsigned char *kdst = my_pipe + slot * C::SLOT_BYTES;
-                unsigned char *vdst = kdst + C::TILE_BYTES;
+                unsigned char *vdst = kdst + C::KV_BYTES;
                 const int row = (id * Hk + pc.j) * bs + (tok0 % bs);
+                if constexpr (F8) {  // a tile of E4M3 rows is contiguous: two bulk copies
+                    const size_t off = static_cast<size_t>(row) * D;
+                    bulk_copy_g2s(kdst, static_cast<const unsigned char *>(a.k_cache) + off,
+                                  C::KV_BYTES, bar);
+                    bulk_copy_g2s(vdst, static_cast<const unsigned char *>(a.v_cache) + off,
+                                  C::KV_BYTES, bar);
+                } else {
 #pragma unroll
-                for (int bx = 0; bx < C::BOXES; ++bx) {
-                    tma_load_2d(kdst + bx * C::BOX_BYTES, &tmap_k, bx * 64, row, bar);
-                    tma_load_2d(vdst + bx * C::BOX_BYTES, &tmap_v, bx * 64, row, bar);
+                    for (int bx = 0; bx < C::BOXES; ++bx) {
+                        tma_load_2d(kdst + bx * C::BOX_BYTES, &tmap_k, bx * 64, row, bar);
+                        tma_load_2d(vdst + bx * C::BOX_BYTES, &tmap_v, bx * 64, row, bar);
+                    }
                 }
             }
             if (newseg)
@@ -337,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsB)
             }
             fm = M;
         }
-        const float inv = fl > 0.f ? 1.f / fl : 0.f;
+        const float inv = fl > 0.f ? a.v_scale / fl : 0.f;  // v_scale = 1 for fp16 caches
         __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
 #pragma unroll
         for (int nb = 0; nb < C::NB_D; ++nb)
@@ -397,7 +444,7 @@ __global__ void __launch_bounds__(kThreadsB)
         const int wf = x0 / U;
         const int wl = (x0 + nt - 1) / U;
         const bool wf_starts_here = wf * U == x0;
-        constexpr int cap = static_cast<int>((kS * C::SLOT_BYTES) / REC);
+        constexpr int cap = static_cast<int>(C::WARP_BYTES / REC);
         float M = -INFINITY, Lsum = 0.f;
 #pragma unroll
         for (int nb = 0; nb < C::NB_D; ++nb) o[nb][0] = o[nb][1] = 0.f;
@@ -466,7 +513,14 @@ __global__ void __launch_bounds__(kThreadsB)
         }
         last_t = cc.t;
         unsigned char *ks = my_pipe + slot * C::SLOT_BYTES;
-        unsigned char *vs = ks + C::TILE_BYTES;
+        unsigned char *vs = ks + C::KV_BYTES;
+        if constexpr (F8) {  // widen the E4M3 tiles into the fp16 layout
+            e4m3_tile_to_f16<D>(ks, my_stage, lane);
+            e4m3_tile_to_f16<D>(vs, my_stage + C::TILE_BYTES, lane);
+            __syncwarp();
+            ks = my_stage;
+            vs = my_stage + C::TILE_BYTES;
+        }
         const int n_valid =
             s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - (cc.t + s_skip[cc.b]) * kMmaTile) : 0;
         mma_tile<D>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
@@ -495,23 +549,23 @@ __global__ void __launch_bounds__(kThreadsB)
     }
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 size_t bal_smem(int B) {
-    using C = BalCfg<D, G>;
+    using C = BalCfg<D, G, F8>;
     return 1024 + C::PIPE_BYTES + C::QS_BYTES + (3 * static_cast<size_t>(B) + 1) * 4;
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 int bal_ctas_per_sm(int B) {
     static std::mutex mu;
     static std::map<size_t, int> cache;
-    const size_t smem = bal_smem<D, G>(B);
+    const size_t smem = bal_smem<D, G, F8>(B);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(smem);
     if (it != cache.end()) return it->second;
-    auto kern = decode_balanced_kernel<D, G>;
+    auto kern = decode_balanced_kernel<D, G, F8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(bal_smem<D, G>(kMaxSeqsBalanced))) != cudaSuccess)
+                             static_cast<int>(bal_smem<D, G, F8>(kMaxSeqsBalanced))) != cudaSuccess)
         return 0;
     // the grid is sized to fill every SM once: ask for the whole carve-out
     if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -524,13 +578,13 @@ int bal_ctas_per_sm(int B) {
     return n;
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t launch_bal_t(const DecodeArgs &a, const BalancedPlan &plan, const CUtensorMap &tk,
                          const CUtensorMap &tv, cudaStream_t stream) {
-    auto kern = decode_balanced_kernel<D, G>;
-    if (bal_ctas_per_sm<D, G>(a.num_seqs) <= 0) return cudaErrorInvalidConfiguration;
-    return launch_pdl(kern, dim3(plan.ctas), dim3(kThreadsB), bal_smem<D, G>(a.num_seqs), stream,
-                      a, tk, tv, plan.workers);
+    auto kern = decode_balanced_kernel<D, G, F8>;
+    if (bal_ctas_per_sm<D, G, F8>(a.num_seqs) <= 0) return cudaErrorInvalidConfiguration;
+    return launch_pdl(kern, dim3(plan.ctas), dim3(kThreadsB), bal_smem<D, G, F8>(a.num_seqs),
+                      stream, a, tk, tv, plan.workers);
 }
 
 int sm_count_cached() {
@@ -554,11 +608,13 @@ bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
 }
 
 bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
-                   BalancedPlan *plan) {
+                   BalancedPlan *plan, bool kv_fp8) {
     const int G = n_q_heads / n_kv_heads;
     int per_sm = 0;
-#define PKV_BAL_OCC(D_, G_) \
-    if (head_dim == D_ && G == G_) per_sm = bal_ctas_per_sm<D_, G_>(num_seqs);
+#define PKV_BAL_OCC(D_, G_)                                                               \
+    if (head_dim == D_ && G == G_)                                                          \
+        per_sm = kv_fp8 ? bal_ctas_per_sm<D_, G_, true>(num_seqs)                          \
+                        : bal_ctas_per_sm<D_, G_, false>(num_seqs);
     PKV_BAL_OCC(128, 1)
     PKV_BAL_OCC(128, 2)
     PKV_BAL_OCC(128, 4)
@@ -588,13 +644,15 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
 cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
                                    cudaStream_t stream) {
     const long long rows = a.num_blocks * a.n_kv_heads * static_cast<long long>(a.block_size);
-    CUtensorMap tk, tv;
-    if (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
-        !make_cache_map(&tv, a.v_cache, rows, a.head_dim))
+    CUtensorMap tk{}, tv{};  // FP8 caches move by plain bulk copies, no tensor map
+    if (!a.kv_fp8 && (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
+                      !make_cache_map(&tv, a.v_cache, rows, a.head_dim)))
         return cudaErrorNotSupported;
     const int g = a.n_q_heads / a.n_kv_heads;
-#define PKV_BAL_CASE(D_, G_) \
-    if (a.head_dim == D_ && g == G_) return launch_bal_t<D_, G_>(a, plan, tk, tv, stream);
+#define PKV_BAL_CASE(D_, G_)                                                       \
+    if (a.head_dim == D_ && g == G_)                                                \
+        return a.kv_fp8 ? launch_bal_t<D_, G_, true>(a, plan, tk, tv, stream)      \
+                        : launch_bal_t<D_, G_, false>(a, plan, tk, tv, stream);
     PKV_BAL_CASE(128, 1)
     PKV_BAL_CASE(128, 2)
     PKV_BAL_CASE(128, 4)

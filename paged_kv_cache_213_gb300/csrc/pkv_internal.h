@@ -83,6 +83,10 @@ struct DecodeArgs {
     // prologue and private tiles before its grid-dependency wait and waits
     // only before it reads those partials.  0: wait first.
     int defer_dep_wait;
+    // FP8 caches (balanced kernel only): k_cache / v_cache hold E4M3 codes,
+    // scale_log2 already includes k_scale, and outputs are multiplied by v_scale
+    int kv_fp8 = 0;
+    float v_scale = 1.f;          // 1 for fp16 caches
 };
 
 // Workspace carve-up shared by the planner and the launcher.
@@ -92,6 +96,9 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts);
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
+// FP8 (E4M3) caches: k_cache / v_cache hold one byte per value, head_dim % 16 == 0.
+cudaError_t launch_append_f8(const AppendArgs &a, float k_scale, float v_scale,
+                             cudaStream_t stream);
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
                                const int32_t *dst, const int32_t *tokens, int num_copies,
                                int n_kv_heads, int head_dim, int block_size, long long num_blocks,
@@ -118,7 +125,7 @@ bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
 // Grid and workspace for the balanced kernel (host query of the SM count
 // and occupancy); false if the device query fails.
 bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
-                   BalancedPlan *plan);
+                   BalancedPlan *plan, bool kv_fp8 = false);
 cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
                                    cudaStream_t stream);
 // Shared-prefix pass (decode_shared.cu): each warp holds 16 query rows.

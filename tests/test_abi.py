@@ -111,3 +111,24 @@ def test_calls_reject_bad_arguments_without_launching(lib):
 def test_auto_plan_needs_a_device(lib):
     rc, _, _ = _plan(lib, 4, 8, 2, 128, 16, 8, 0, 0)
     assert rc == -4
+
+
+def test_fp8_host_rejections(lib):
+    import ctypes as c
+    p = c.c_void_p
+    fn = lib.paged_kv_append_fp8
+    fn.argtypes = [p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_float,
+                   c.c_float, p, p]
+    fn.restype = c.c_int
+    x = p(256)
+    # head_dim not a multiple of 16, a zero scale, a NaN scale: rejected before any launch
+    assert fn(x, x, x, x, x, 4, 2, 8, 16, 10, 1.0, 1.0, None, None) == -1
+    assert fn(x, x, x, x, x, 4, 2, 64, 16, 10, 0.0, 1.0, None, None) == -1
+    assert fn(x, x, x, x, x, 4, 2, 64, 16, 10, 1.0, float("nan"), None, None) == -1
+    att = lib.paged_decode_attention_fp8
+    att.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float, c.c_float,
+                    c.c_float, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p,
+                    p]
+    att.restype = c.c_int
+    assert att(x, x, x, x, x, x, 4, 8, 10, 0.1, -1.0, 1.0, 8, 2, 128, 16, 0, x, 1 << 20, None,
+               None, None) == -1
