@@ -59,6 +59,8 @@ def parse_args(argv=None):
                     help="CPU-oracle sample length for cpu_baseline")
     ap.add_argument("--prefix-shared", action="store_true",
                     help="use the prefix-aware entry point (workloads with shared prefixes)")
+    ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
+                    help="cache element type: fp16, or E4M3 codes with per-tensor scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -173,9 +175,9 @@ def gpu_selector(torch, device) -> str:
 # byte accounting
 # ----------------------------------------------------------------------------
 
-def workload_bytes(batch):
+def workload_bytes(batch, kv_bytes=2):
     from paged_kv_cache_213_gb300 import workloads as wl
-    s = wl.stats(batch)
+    s = wl.stats(batch, kv_bytes)
     attn = s["unique_kv"] + s["qo"] + s["meta"]
     return {"step": s["step_unique"], "attention": attn, "append": s["append"],
             "logical_step": s["step_logical"], "stats": s}
@@ -280,12 +282,23 @@ def run_ours(args):
     pkv.library()  # raises if the CUDA library is not built
 
     batch = wl.workload(args.workload, poison=False)
-    nbytes = workload_bytes(batch)
+    fp8 = args.kv_dtype == "fp8"
+    nbytes = workload_bytes(batch, 1 if fp8 else 2)
 
     def t(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
     q, kc, vc = t(batch.q), t(batch.k_cache), t(batch.v_cache)
+    k_scale = v_scale = 1.0
+    if fp8:
+        # per-tensor scales max|x| / 448; the caches' E4M3 codes made by torch
+        # (input preparation, outside the timed path)
+        def amax(*xs):
+            return max(float(np.max(np.abs(x.astype(np.float32)))) for x in xs)
+        k_scale = np.float32(amax(batch.k_cache, *([batch.k_new] if batch.has_append else [])) / 448)
+        v_scale = np.float32(amax(batch.v_cache, *([batch.v_new] if batch.has_append else [])) / 448)
+        kc = (kc.float() / float(k_scale)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        vc = (vc.float() / float(v_scale)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
     bt, cl = t(batch.block_tables), t(batch.context_lens)
     has_append = batch.has_append
     if has_append:
@@ -297,10 +310,12 @@ def run_ours(args):
     mcl = batch.max_context_len
     P, ws_bytes = pkv.decode_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
                                   args.partition)
+    if fp8:
+        P, ws_bytes = 0, pkv.decode_plan_fp8(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl)
     # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
     launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 and P > 0 else 0)
     groups = None
-    if args.prefix_shared and batch.meta.get("shared"):
+    if args.prefix_shared and batch.meta.get("shared") and not fp8:
         offs, pref, gmax, pmax = wl.prefix_groups(batch)
         groups = (t(offs), t(pref), gmax, pmax)
         ws_bytes = pkv.prefix_shared_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
@@ -318,10 +333,17 @@ def run_ours(args):
         torch.sum(flush_r, dim=0, out=sink[0])
 
     def append():
-        if has_append:
+        if has_append and fp8:
+            pkv.paged_kv_append_fp8(kn, vn, sm, kc, vc, k_scale, v_scale, err_word=err)
+        elif has_append:
             pkv.paged_kv_append(kn, vn, sm, kc, vc, err_word=err)
 
     def attend():
+        if fp8:
+            pkv.paged_decode_attention_fp8(q, kc, vc, bt, cl, batch.scale, k_scale, v_scale, H,
+                                           Hk, D, bs, max_context_len=mcl, out=out,
+                                           workspace=work, err_word=err)
+            return
         if groups is not None:
             pkv.paged_decode_attention_prefix_shared(
                 q, kc, vc, bt, cl, batch.scale, H, Hk, D, bs, groups[0], groups[1], groups[2],
@@ -463,9 +485,9 @@ def run_ours(args):
 
     peak, peak_src = load_peak()
     achieved = nbytes["attention"] / (attn_ms_mean * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    traffic = None if fp8 else ncu_traffic(args.workload)  # the summary covers the fp16 kernel
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not fp8:
         cpu = cpu_baseline(batch, args.cpu_seconds)
 
     if rank != 0:
@@ -488,6 +510,7 @@ def run_ours(args):
             "decode_kernel": os.environ.get("PKV_DECODE_KERNEL",
                                             "auto (tensor-core kernel when block_size % 16 == 0)"),
             "prefix_shared": groups is not None,
+            "kv_dtype": "e4m3 (per-tensor scales)" if fp8 else "f16",
         },
         "steps_per_sec": round(1e3 / step_ms, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),

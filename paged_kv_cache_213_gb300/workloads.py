@@ -229,12 +229,14 @@ def workload(i: int, poison: bool = False, seed: int | None = None) -> PagedBatc
     raise ValueError(f"unknown workload {i}")
 
 
-def stats(batch: PagedBatch) -> dict:
+def stats(batch: PagedBatch, kv_bytes: int = 2) -> dict:
     """Byte counts of one decode step (element counts times element sizes).
 
     unique_kv: K+V bytes of every (physical block, KV head) row some sequence
       reads, each counted once -- what the step must move from HBM.
     logical_kv: K+V bytes gathered per sequence, sum over sequences.
+    kv_bytes: bytes per cached value (2 for fp16, 1 for E4M3 codes); the
+      append reads fp16 k_new / v_new and writes kv_bytes per value.
     """
     bs, d, Hk = batch.block_size, batch.head_dim, batch.n_kv_heads
     rows = set()
@@ -249,13 +251,14 @@ def stats(batch: PagedBatch) -> dict:
         reach[blk] = max(reach.get(blk, 0), n)
     unique_tokens = sum(reach.values())
     logical_tokens = int(batch.context_lens.astype(np.int64).sum())
-    per_token = 2 * Hk * d * 2
+    per_token = 2 * Hk * d * kv_bytes
     B, H = batch.num_seqs, batch.n_q_heads
     qo = 2 * B * H * d * 2
     meta = batch.block_tables.nbytes + batch.context_lens.nbytes
     app = 0
     if batch.has_append:
-        app = 2 * batch.k_new.nbytes + 2 * batch.v_new.nbytes + batch.slot_mapping.nbytes
+        new_bytes = batch.k_new.nbytes + batch.v_new.nbytes
+        app = new_bytes + new_bytes * kv_bytes // 2 + batch.slot_mapping.nbytes
     return {
         "unique_kv": unique_tokens * per_token,
         "logical_kv": logical_tokens * per_token,
