@@ -20,6 +20,9 @@ What each function follows (page title, section):
     written into their assigned physical block slot.
   * ``partial`` / ``lse_merge`` -- the log-sum-exp split of the same softmax
     (FlashAttention-2, cited in section 14 of that page).
+  * ``decode_multi`` -- several new tokens per sequence attending causally
+    over the paged cache (speculative-decoding verify and chunked prefill:
+    the roadmap page's Deferred list, and section 9.2 of the serving page).
   * ``e4m3_*``, ``append_f8``, ``decode_f8`` -- the FP8 KV cache that
     "Roadmap: vLLM-style serving features for TornadoVM batched decode" (KV
     cache list) names as future work; the format (OCP E4M3, per-tensor
@@ -89,6 +92,9 @@ def _bind(lib):
                                    c.c_int64, c.c_double, c.c_int, c.c_int, c.c_int, c.c_int, p,
                                    p, p, c.c_int]
     lib.pkvo_decode_f8.restype = c.c_int
+    lib.pkvo_decode_multi.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_double,
+                                      c.c_int, c.c_int, c.c_int, c.c_int, p, p, c.c_int]
+    lib.pkvo_decode_multi.restype = c.c_int
     return lib
 
 
@@ -297,4 +303,39 @@ def decode_f8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, context_len
                             _ptr(out), _ptr(lse), int(num_threads))
     if rc != 0:
         raise OracleError("invalid decode input")
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# multi-token (causal) paged attention
+# ---------------------------------------------------------------------------
+
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                 n_q_heads, n_kv_heads, head_dim, block_size, num_threads=0, lib=None):
+    """Causal attention of each sequence's last n_b tokens over its paged K/V.
+
+    q: [total_q, H, d] fp16, query rows [query_start[b], query_start[b+1]) of
+    sequence b at positions L_b - n_b + i.  Returns (out f64 [total_q, H, d],
+    lse f64 [total_q, H]).
+    """
+    lib = lib or load()
+    q = _u16(q)
+    kc, vc = _u16(k_cache), _u16(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    B = cl.shape[0]
+    TQ, H, d = q.shape
+    NB = kc.shape[0]
+    if (H, d) != (n_q_heads, head_dim) or kc.shape != (NB, n_kv_heads, block_size, head_dim):
+        raise ValueError("shape mismatch")
+    if vc.shape != kc.shape or bt.shape[0] != B or qs.shape != (B + 1,) or qs[-1] != TQ:
+        raise ValueError("shape mismatch")
+    out = np.full((TQ, H, d), np.nan)
+    lse = np.full((TQ, H), np.nan)
+    rc = lib.pkvo_decode_multi(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl), _ptr(qs), B,
+                               bt.shape[1], NB, float(scale), n_q_heads, n_kv_heads, head_dim,
+                               block_size, _ptr(out), _ptr(lse), int(num_threads))
+    if rc != 0:
+        raise OracleError("invalid multi-token input")
     return out, lse

@@ -476,3 +476,100 @@ void pkvo_f32_to_e4m3_array(const float *y, int64_t n, uint8_t *codes)
 {
     for (int64_t i = 0; i < n; ++i) codes[i] = pkvo_f32_to_e4m3(y[i]);
 }
+
+/* ---------------------------------------------------------------------------
+ * Multi-token paged attention (speculative-decoding verify, chunked prefill).
+ * "Roadmap: vLLM-style serving features for TornadoVM batched decode",
+ * Deferred list (batch-prefill verify of draft tokens; multi-token chunked
+ * prefill) and "Distributed LLM Inference Serving Platform", section 9.2
+ * (chunked prefill): several new tokens of one sequence attend in one step.
+ * Reading (listed in the design notes): sequence b contributes the query
+ * rows [query_start[b], query_start[b+1]) of q; these n_b tokens are the last
+ * n_b of its context_lens[b] = L cached tokens (already appended), so query
+ * token i sits at position L - n_b + i and attends the tokens [0, L - n_b + i]
+ * (causal).  q, out: [total_q][n_q_heads][head_dim]; lse: [total_q][n_q_heads].
+ * ------------------------------------------------------------------------- */
+
+/* attend_range with the query vector given directly (qv) instead of by (b, h). */
+static int attend_range_qv(const uint16_t *qv, const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           int64_t num_blocks, double scale, int n_q_heads, int n_kv_heads,
+                           int head_dim, int block_size, int b, int h, int t_begin, int t_end,
+                           double *m_out, double *l_out, double *acc)
+{
+    int group = n_q_heads / n_kv_heads;
+    int j = h / group;
+    int n = t_end - t_begin;
+    for (int k = 0; k < head_dim; ++k) acc[k] = 0.0;
+    *m_out = -INFINITY;
+    *l_out = 0.0;
+    if (n <= 0) return 0;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!s) return -2;
+    for (int t = t_begin; t < t_end; ++t) {
+        const uint16_t *kt = token_row(k_cache, block_tables, max_blocks_per_seq, num_blocks,
+                                       n_kv_heads, head_dim, block_size, b, j, t);
+        if (!kt) { free(s); return -1; }
+        double dot = 0.0;
+        for (int k = 0; k < head_dim; ++k) dot += g_f16[qv[k]] * g_f16[kt[k]];
+        s[t - t_begin] = scale * dot;
+    }
+    double m = -INFINITY;
+    for (int i = 0; i < n; ++i) if (s[i] > m) m = s[i];
+    double l = 0.0;
+    for (int i = 0; i < n; ++i) { s[i] = exp(s[i] - m); l += s[i]; }
+    for (int t = t_begin; t < t_end; ++t) {
+        const uint16_t *vt = token_row(v_cache, block_tables, max_blocks_per_seq, num_blocks,
+                                       n_kv_heads, head_dim, block_size, b, j, t);
+        double p = s[t - t_begin];
+        for (int k = 0; k < head_dim; ++k) acc[k] += p * g_f16[vt[k]];
+    }
+    free(s);
+    *m_out = m;
+    *l_out = l;
+    return 0;
+}
+
+int pkvo_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      const int32_t *query_start, int num_seqs, int max_blocks_per_seq,
+                      int64_t num_blocks, double scale, int n_q_heads, int n_kv_heads,
+                      int head_dim, int block_size, double *out, double *lse, int num_threads)
+{
+    f16_table_init();
+    if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -1;
+    if (query_start[0] != 0) return -1;
+    for (int b = 0; b < num_seqs; ++b) {
+        int L = context_lens[b];
+        int nq = query_start[b + 1] - query_start[b];
+        if (L < 0 || L > max_blocks_per_seq * block_size) return -1;
+        if (nq < 0 || nq > L) return -1;
+    }
+    int total_q = query_start[num_seqs];
+    int failed = 0;
+    int64_t rows = (int64_t)total_q * n_q_heads;
+#ifdef _OPENMP
+    int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt) reduction(| : failed)
+#endif
+    for (int64_t rh = 0; rh < rows; ++rh) {
+        int r = (int)(rh / n_q_heads);
+        int h = (int)(rh % n_q_heads);
+        int b = 0;
+        while (query_start[b + 1] <= r) ++b;          /* the sequence of query row r */
+        int nq = query_start[b + 1] - query_start[b];
+        int pos = context_lens[b] - nq + (r - query_start[b]);   /* its position */
+        double *acc = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        double m, l;
+        int rc = attend_range_qv(q + rh * head_dim, k_cache, v_cache, block_tables,
+                                 max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
+                                 head_dim, block_size, b, h, 0, pos + 1, &m, &l, acc);
+        if (rc != 0) { failed = 1; free(acc); continue; }
+        for (int k = 0; k < head_dim; ++k)
+            if (out) out[rh * head_dim + k] = (l > 0.0) ? acc[k] / l : 0.0;
+        if (lse) lse[rh] = (l > 0.0) ? m + log(l) : -INFINITY;
+        free(acc);
+    }
+    (void)num_threads;
+    return failed ? -1 : 0;
+}

@@ -556,7 +556,114 @@ def pin_f8_poison(lib, seed=24):
     assert np.all(np.isfinite(a[0])) and np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+# ----------------------------------------------------------------------------
+# multi-token (causal) paged attention pins
+# ----------------------------------------------------------------------------
+
+def multi_problem(rng, B, H, Hk, d, lens, nq):
+    """Logical K/V [B, Hk, Lmax, d] and packed queries [sum(nq), H, d]."""
+    lens = np.asarray(lens)
+    K = randn16(rng, (B, Hk, int(lens.max()), d))
+    V = randn16(rng, (B, Hk, int(lens.max()), d))
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = randn16(rng, (int(qs[-1]), H, d))
+    return q, K, V, lens, qs
+
+
+def dense_causal_reference(q, K, V, lens, qs, scale, H, Hk):
+    """float64 torch SDPA with an explicit causal mask aligned to the end of
+    each sequence, and scipy's logsumexp over the same masked logits."""
+    TQ, _, d = q.shape
+    g = H // Hk
+    out = np.zeros((TQ, H, d))
+    lse = np.full((TQ, H), -np.inf)
+    for b in range(len(lens)):
+        L = int(lens[b])
+        r0, r1 = int(qs[b]), int(qs[b + 1])
+        n = r1 - r0
+        if n == 0:
+            continue
+        qt = torch.from_numpy(q[r0:r1].astype(np.float64)).permute(1, 0, 2).reshape(1, H, n, d)
+        kt = torch.from_numpy(K[b, :, :L].astype(np.float64)).repeat_interleave(g, dim=0)
+        vt = torch.from_numpy(V[b, :, :L].astype(np.float64)).repeat_interleave(g, dim=0)
+        pos = np.arange(n)[:, None] + (L - n)
+        allowed = np.arange(L)[None, :] <= pos
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt.reshape(1, H, L, d), vt.reshape(1, H, L, d),
+            attn_mask=torch.from_numpy(allowed), scale=scale)
+        out[r0:r1] = o.reshape(H, n, d).permute(1, 0, 2).numpy()
+        s = np.einsum("nhd,hld->nhl", q[r0:r1].astype(np.float64), kt.numpy()) * scale
+        s = np.where(allowed[:, None, :], s, -np.inf)
+        lse[r0:r1] = scipy.special.logsumexp(s, axis=2)
+    return out, lse
+
+
+def pin_multi_dense(lib, seed=31):
+    """Multi-token paged attention = causal float64 SDPA on contiguous K/V."""
+    rng = np.random.default_rng(seed)
+    for (B, H, Hk, d, bs, lens, nq) in [(3, 4, 2, 64, 16, (5, 17, 40), (1, 4, 8)),
+                                        (2, 8, 2, 128, 16, (33, 16), (16, 3)),
+                                        (3, 4, 4, 64, 1, (9, 3, 6), (2, 3, 0)),
+                                        (2, 8, 1, 64, 8, (64, 20), (5, 20))]:
+        q, K, V, lens, qs = multi_problem(rng, B, H, Hk, d, lens, nq)
+        scale = 1.0 / math.sqrt(d)
+        kc, vc, bt = paginate(K, V, lens, bs, rng)
+        out, lse = oracle.decode_multi(q, kc, vc, bt, lens.astype(np.int32), qs, scale, H, Hk,
+                                       d, bs, lib=lib)
+        ref, ref_lse = dense_causal_reference(q, K, V, lens, qs, scale, H, Hk)
+        assert np.max(np.abs(out - ref)) <= 1e-12, np.max(np.abs(out - ref))
+        assert np.max(np.abs(lse - ref_lse)) <= 1e-12
+
+
+def pin_multi_is_truncated_decode(lib, seed=32):
+    """Query token i of a sequence equals a one-token decode of the same query
+    over the context cut at its position (bitwise); one query per sequence is
+    exactly the decode."""
+    rng = np.random.default_rng(seed)
+    B, H, Hk, d, bs = 3, 4, 2, 64, 16
+    q, K, V, lens, qs = multi_problem(rng, B, H, Hk, d, (12, 33, 7), (3, 5, 7))
+    kc, vc, bt = paginate(K, V, lens, bs, rng)
+    out, lse = oracle.decode_multi(q, kc, vc, bt, lens.astype(np.int32), qs, 0.125, H, Hk, d,
+                                   bs, lib=lib)
+    for b in range(B):
+        n = int(qs[b + 1] - qs[b])
+        for i in range(n):
+            cut = lens.copy()
+            cut[b] = lens[b] - n + i + 1
+            qd = np.repeat(q[qs[b] + i][None], B, axis=0)
+            o1, l1, _ = run_decode(lib, qd, kc, vc, bt, cut, 0.125, H, Hk, d, bs)
+            assert np.array_equal(out[qs[b] + i], o1[b]) and np.array_equal(lse[qs[b] + i], l1[b])
+    ones = np.arange(B + 1, dtype=np.int32)
+    q1 = q[:B]
+    o_m, l_m = oracle.decode_multi(q1, kc, vc, bt, lens.astype(np.int32), ones, 0.125, H, Hk, d,
+                                   bs, lib=lib)
+    o_d, l_d, _ = run_decode(lib, q1, kc, vc, bt, lens, 0.125, H, Hk, d, bs)
+    assert np.array_equal(o_m, o_d) and np.array_equal(l_m, l_d)
+
+
+def pin_multi_poison_and_rejects(lib, seed=33):
+    rng = np.random.default_rng(seed)
+    B, H, Hk, d, bs = 2, 4, 2, 64, 16
+    q, K, V, lens, qs = multi_problem(rng, B, H, Hk, d, (17, 30), (4, 2))
+    kc, vc, bt = paginate(K, V, lens, bs, np.random.default_rng(2), poison=False)
+    kc2, vc2, bt2 = paginate(K, V, lens, bs, np.random.default_rng(2), poison=True)
+    a = oracle.decode_multi(q, kc, vc, bt, lens.astype(np.int32), qs, 0.125, H, Hk, d, bs,
+                            lib=lib)
+    b = oracle.decode_multi(q, kc2, vc2, bt2, lens.astype(np.int32), qs, 0.125, H, Hk, d, bs,
+                            lib=lib)
+    assert np.all(np.isfinite(a[0])) and np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    bad = lens.copy()
+    bad[0] = 3  # fewer cached tokens than query tokens
+    try:
+        oracle.decode_multi(q, kc, vc, bt, bad.astype(np.int32), qs, 0.125, H, Hk, d, bs, lib=lib)
+    except oracle.OracleError:
+        pass
+    else:
+        raise AssertionError("more query tokens than context accepted")
+
+
 ALL_PINS = [pin_fp16_decode, pin_fp16_encode, pin_dense_sdpa, pin_closed_forms,
             pin_invariances, pin_merge, pin_poison, pin_append, pin_append_then_attend,
             pin_rejects_bad_input, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_quantize,
-            pin_f8_dense, pin_f8_append, pin_f8_poison]
+            pin_f8_dense, pin_f8_append, pin_f8_poison, pin_multi_dense,
+            pin_multi_is_truncated_decode, pin_multi_poison_and_rejects]

@@ -44,6 +44,13 @@ MUTANTS = [
     ("f8_quantize_multiplies", "volatile float y = x / scale;", "volatile float y = x * scale;"),
     ("f8_k_scale_dropped", "(g_e4m3[kt[k]] * k_scale)", "g_e4m3[kt[k]]"),
     ("f8_v_scale_dropped", "acc[k] += p * (g_e4m3[vt[k]] * v_scale);", "acc[k] += p * g_e4m3[vt[k]];"),
+    ("multi_causal_one_past", "b, h, 0, pos + 1, &m, &l, acc);", "b, h, 0, pos + 2, &m, &l, acc);"),
+    ("multi_no_causal_mask", "int pos = context_lens[b] - nq + (r - query_start[b]);",
+     "int pos = context_lens[b] - 1;"),
+    ("multi_position_from_start", "int pos = context_lens[b] - nq + (r - query_start[b]);",
+     "int pos = r - query_start[b];"),
+    ("multi_first_query_row", "rc = attend_range_qv(q + rh * head_dim,",
+     "rc = attend_range_qv(q + ((int64_t)query_start[b] * n_q_heads + h) * head_dim,"),
     ("empty_range_bound", "for (int t = t_begin; t < t_end; ++t) {\n        const uint16_t *kt",
      "for (int t = t_begin; t < t_end - (t_end - t_begin > 1); ++t) {\n        const uint16_t *kt"),
 ]
