@@ -253,6 +253,46 @@ int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
                                float *lse_out, int32_t *err_word, void *cuda_stream);
 
 /*
+ * Multi-token (causal) paged attention: several new tokens of each sequence
+ * attend in one call -- verifying speculative draft tokens, or a chunk of a
+ * chunked prefill ("Roadmap: vLLM-style serving features for TornadoVM
+ * batched decode", Deferred list: batch-prefill verify, multi-token chunked
+ * prefill; "Distributed LLM Inference Serving Platform", section 9.2).
+ *  q, out       fp16 [total_q][n_q_heads][head_dim]; lse_out fp32
+ *               [total_q][n_q_heads] (nullable)
+ *  query_start  device int32 [num_seqs + 1], query_start[0] = 0,
+ *               query_start[num_seqs] = total_q: sequence b owns the query
+ *               rows [query_start[b], query_start[b+1]), n_b of them
+ *  context_lens device int32 [num_seqs]: cached tokens L_b, the n_b new
+ *               tokens included (append them first); n_b <= L_b
+ * Query token i of sequence b sits at position L_b - n_b + i and attends the
+ * tokens [0, L_b - n_b + i] of its block table (causal); n_b = 1 is the
+ * decode of paged_decode_attention.  max_q_len: host upper bound of n_b
+ * (grid sizing; rows past it are not computed).  partition_tokens: KV tokens
+ * per split-K partition (0 = the library's choice, else a multiple of 16 and
+ * of block_size); paged_decode_multi_plan gives it and the workspace bytes
+ * (0 when one partition covers max_context_len; no zero-fill needed).
+ * Requirements: block_size a multiple of 16, head_dim 64 or 128, n_q/n_kv in
+ * {1, 2, 4, 8} (PKV_ERR_UNSUPPORTED otherwise).  A sequence with n_b > L_b or
+ * rows outside [0, total_q) sets PKV_ERRBIT_CONTEXT and its rows are left
+ * unwritten.  Other arguments, errors and ownership as for
+ * paged_decode_attention.
+ */
+int paged_decode_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads,
+                            int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                            int max_context_len, int partition_tokens, int *partition_tokens_out,
+                            size_t *workspace_bytes_out);
+int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, const int32_t *query_start,
+                                 int num_seqs, int total_q, int max_q_len,
+                                 int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                 int max_context_len, int partition_tokens, void *workspace,
+                                 size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                                 void *cuda_stream);
+
+/*
  * Allocation-free variant of paged_decode_attention.  The pages have no
  * counterpart to this call.  It serves callers that cannot allocate device
  * memory and so cannot supply the split-K workspace: an operator running

@@ -18,8 +18,10 @@ from .binding import (  # noqa: F401
     get_error,
     library,
     library_path,
+    multi_plan,
     paged_decode_attention,
     paged_decode_attention_fp8,
+    paged_decode_attention_multi,
     paged_decode_attention_prefix_shared,
     paged_kv_append,
     paged_kv_append_fp8,

@@ -433,3 +433,77 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, 
                 _stream_handle(dev))
     _check("paged_decode_attention_fp8", rc)
     return out
+
+
+# ---------------------------------------------------------------------------
+# multi-token (causal) attention: speculative verify, chunked prefill
+# ---------------------------------------------------------------------------
+
+def multi_plan(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim, block_size,
+               max_blocks_per_seq, max_context_len=0, partition_tokens=0):
+    """(partition_tokens, workspace_bytes) of paged_decode_attention_multi."""
+    lib = library()
+    fn = lib.paged_decode_multi_plan
+    c = ctypes
+    fn.argtypes = [c.c_int] * 10 + [c.POINTER(c.c_int), c.POINTER(c.c_size_t)]
+    fn.restype = c.c_int
+    P = c.c_int(0)
+    W = c.c_size_t(0)
+    _check("paged_decode_multi_plan",
+           fn(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim, block_size,
+              max_blocks_per_seq, max_context_len, partition_tokens, c.byref(P), c.byref(W)))
+    return P.value, W.value
+
+
+def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, query_start,
+                                 scale, n_q_heads, n_kv_heads, head_dim, block_size, max_q_len,
+                                 max_context_len=None, partition_tokens=0, out=None,
+                                 workspace=None, lse=None, err_word=None):
+    """Causal attention of each sequence's last n_b tokens over its paged K/V.
+
+    q [total_q, H, d] fp16 (sequence b owns rows [query_start[b], query_start[b+1]));
+    query_start [B + 1] int32; context_lens include the new tokens.  Returns
+    out [total_q, H, d] fp16."""
+    lib = library()
+    fn = lib.paged_decode_attention_multi
+    c = ctypes
+    p = c.c_void_p
+    fn.argtypes = [p, p, p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_float,
+                   c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p, p]
+    fn.restype = c.c_int
+    dev = q.device
+    for t, name, dt in ((q, "q", torch.float16), (k_cache, "k_cache", torch.float16),
+                        (v_cache, "v_cache", torch.float16),
+                        (block_tables, "block_tables", torch.int32),
+                        (context_lens, "context_lens", torch.int32),
+                        (query_start, "query_start", torch.int32)):
+        _need(t, name, dt, dev)
+    B, MB = block_tables.shape
+    TQ = q.shape[0]
+    if q.dim() != 3 or q.shape[1:] != (n_q_heads, head_dim):
+        raise ValueError("q must be [total_q, n_q_heads, head_dim]")
+    if query_start.shape != (B + 1,) or context_lens.shape != (B,):
+        raise ValueError("query_start must be [B + 1], context_lens [B]")
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    P, ws = multi_plan(B, TQ, int(max_q_len), n_q_heads, n_kv_heads, head_dim, block_size, MB,
+                       mcl, partition_tokens)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, dev)
+    if ws > 0:
+        if workspace is None:
+            workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                _ptr(context_lens), _ptr(query_start), B, TQ, int(max_q_len), MB,
+                k_cache.shape[0], float(scale), n_q_heads, n_kv_heads, head_dim, block_size, mcl,
+                P, _ptr(workspace) if ws > 0 else None, workspace.numel() if ws > 0 else 0,
+                _ptr(lse), _ptr(err_word), _stream_handle(dev))
+    _check("paged_decode_attention_multi", rc)
+    return out

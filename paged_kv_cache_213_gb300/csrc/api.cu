@@ -463,6 +463,136 @@ int paged_decode_attention_prefix_shared(
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+struct MultiPlan {
+    int max_len, partition, max_parts, row_blocks;
+    size_t ws_bytes;
+};
+
+int make_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads, int n_kv_heads,
+                    int head_dim, int block_size, int max_blocks_per_seq, int max_context_len,
+                    int partition_tokens, MultiPlan *mp) {
+    if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || n_q_heads <= 0 || n_kv_heads <= 0 ||
+        head_dim <= 0 || max_blocks_per_seq <= 0 || n_q_heads % n_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (block_size % 16 != 0 || !block_size_ok(block_size)) return PKV_ERR_UNSUPPORTED;
+    const int group = n_q_heads / n_kv_heads;
+    if ((head_dim != 64 && head_dim != 128) ||
+        (group != 1 && group != 2 && group != 4 && group != 8))
+        return PKV_ERR_UNSUPPORTED;
+    const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+    if (cap > (1LL << 30)) return PKV_ERR_INVALID_ARG;
+    long long max_len = max_context_len <= 0 ? cap : max_context_len;
+    if (max_len > cap) max_len = cap;
+    mp->max_len = static_cast<int>(max_len);
+    mp->row_blocks = pkv::multi_row_blocks(max_q_len > 0 ? max_q_len : 1, group);
+    int P = partition_tokens;
+    if (P == 0) {
+        // the largest power of two in [64, 2048] whose grid still has about
+        // eight warps per SM
+        int sms = 0;
+        const int rc = sm_count(&sms);
+        if (rc != PKV_OK) return rc;
+        P = 2048;
+        const long long items = static_cast<long long>(num_seqs) * n_kv_heads * mp->row_blocks;
+        while (P > 64 && items * ((max_len + P - 1) / P) < 8LL * sms) P /= 2;
+    } else if (P < 16 || P % 16 != 0 || P % block_size != 0) {
+        return PKV_ERR_INVALID_ARG;
+    }
+    const long long parts = max_len > 0 ? (max_len + P - 1) / P : 1;
+    if (parts > 65535) return PKV_ERR_UNSUPPORTED;
+    mp->partition = P;
+    mp->max_parts = static_cast<int>(parts);
+    mp->ws_bytes = mp->max_parts > 1
+                       ? pkv::workspace_layout(total_q, n_q_heads, head_dim, mp->max_parts).total
+                       : 0;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_decode_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads,
+                            int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                            int max_context_len, int partition_tokens, int *partition_tokens_out,
+                            size_t *workspace_bytes_out) {
+    MultiPlan mp{};
+    const int rc = make_multi_plan(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim,
+                                   block_size, max_blocks_per_seq, max_context_len,
+                                   partition_tokens, &mp);
+    if (rc != PKV_OK) return rc;
+    if (partition_tokens_out) *partition_tokens_out = mp.partition;
+    if (workspace_bytes_out) *workspace_bytes_out = mp.ws_bytes;
+    return PKV_OK;
+}
+
+int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, const int32_t *query_start,
+                                 int num_seqs, int total_q, int max_q_len,
+                                 int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                 int max_context_len, int partition_tokens, void *workspace,
+                                 size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                                 void *cuda_stream) {
+    if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    MultiPlan mp{};
+    int rc = make_multi_plan(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim,
+                             block_size, max_blocks_per_seq, max_context_len, partition_tokens,
+                             &mp);
+    if (rc != PKV_OK) return rc;
+    if (num_seqs == 0 || total_q == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(query_start, 4) ||
+        (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
+        return PKV_ERR_INVALID_ARG;
+    if (mp.ws_bytes > 0 &&
+        (!workspace || workspace_bytes < mp.ws_bytes || !aligned(workspace, 256)))
+        return PKV_ERR_WORKSPACE;
+    if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
+        return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+    pkv::DecodeArgs a{};
+    if (mp.ws_bytes > 0) {
+        const pkv::WorkspaceLayout w =
+            pkv::workspace_layout(total_q, n_q_heads, head_dim, mp.max_parts);
+        char *base = static_cast<char *>(workspace);
+        a.ws_acc = reinterpret_cast<float *>(base + w.acc_offset);
+        a.ws_m = reinterpret_cast<float *>(base + w.m_offset);
+        a.ws_l = reinterpret_cast<float *>(base + w.l_offset);
+    }
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.lse_out = lse_out;
+    a.err = err_word;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.max_context_len = mp.max_len;
+    a.partition_tokens = mp.partition;
+    a.max_parts = mp.max_parts;
+    a.query_start = query_start;
+    a.total_q = total_q;
+    const cudaError_t e = pkv::launch_decode_multi(a, mp.row_blocks,
+                                                   static_cast<cudaStream_t>(cuda_stream));
+    if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits_out) {
     if (!err_word) return PKV_ERR_INVALID_ARG;
     int32_t host = 0;

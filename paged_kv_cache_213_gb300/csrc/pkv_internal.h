@@ -87,6 +87,10 @@ struct DecodeArgs {
     // scale_log2 already includes k_scale, and outputs are multiplied by v_scale
     int kv_fp8 = 0;
     float v_scale = 1.f;          // 1 for fp16 caches
+    // multi-token attention: q, out, lse rows are query tokens; sequence b owns
+    // rows [query_start[b], query_start[b+1]) (its last tokens, causal)
+    const int32_t *query_start = nullptr;
+    int total_q = 0;
 };
 
 // Workspace carve-up shared by the planner and the launcher.
@@ -133,5 +137,10 @@ int shared_members_per_warp(int group);
 int shared_max_warps();
 int shared_ctas_per_sm(int head_dim, int group, int warps);
 cudaError_t launch_decode_shared(const DecodeArgs &a, cudaStream_t stream);
+// Multi-token causal attention (decode_multi.cu): grid (max_parts, Hk x row
+// blocks, B) plus the merge kernel when max_parts > 1; workspace as
+// workspace_layout(total_q, n_q_heads, head_dim, max_parts).
+int multi_row_blocks(int max_q_len, int group);
+cudaError_t launch_decode_multi(const DecodeArgs &a, int row_blocks, cudaStream_t stream);
 
 }  // namespace pkv
