@@ -61,6 +61,9 @@ def parse_args(argv=None):
                     help="use the prefix-aware entry point (workloads with shared prefixes)")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="cache element type: fp16, or E4M3 codes with per-tensor scales")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence: > 1 times the multi-token causal call "
+                         "(speculative verify) instead of the decode step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -283,12 +286,25 @@ def run_ours(args):
 
     batch = wl.workload(args.workload, poison=False)
     fp8 = args.kv_dtype == "fp8"
+    nq = max(1, args.q_len)
+    multi = nq > 1
+    if multi:
+        # n new tokens per sequence, already in the cache: an attention-only step
+        # whose Q and O carry n rows per sequence
+        batch.slot_mapping = batch.k_new = batch.v_new = None
+        rng_q = np.random.default_rng(20300 + args.workload)
+        q_multi = rng_q.standard_normal((batch.num_seqs * nq, batch.n_q_heads,
+                                         batch.head_dim)).astype(np.float16)
     nbytes = workload_bytes(batch, 1 if fp8 else 2)
+    if multi:
+        extra = 2 * (nq - 1) * batch.num_seqs * batch.n_q_heads * batch.head_dim * 2
+        for key in ("step", "attention", "logical_step"):
+            nbytes[key] += extra
 
     def t(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
-    q, kc, vc = t(batch.q), t(batch.k_cache), t(batch.v_cache)
+    q, kc, vc = t(q_multi if multi else batch.q), t(batch.k_cache), t(batch.v_cache)
     k_scale = v_scale = 1.0
     if fp8:
         # per-tensor scales max|x| / 448; the caches' E4M3 codes made by torch
@@ -312,6 +328,9 @@ def run_ours(args):
                                   args.partition)
     if fp8:
         P, ws_bytes = 0, pkv.decode_plan_fp8(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl)
+    if multi:
+        qstart = t(np.arange(B + 1, dtype=np.int32) * nq)
+        P, ws_bytes = pkv.multi_plan(B, B * nq, nq, H, Hk, D, bs, batch.max_blocks_per_seq, mcl)
     # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
     launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 and P > 0 else 0)
     groups = None
@@ -339,6 +358,12 @@ def run_ours(args):
             pkv.paged_kv_append(kn, vn, sm, kc, vc, err_word=err)
 
     def attend():
+        if multi:
+            pkv.paged_decode_attention_multi(q, kc, vc, bt, cl, qstart, batch.scale, H, Hk, D,
+                                             bs, nq, max_context_len=mcl, partition_tokens=P,
+                                             out=out, workspace=work if ws_bytes > 0 else None,
+                                             err_word=err)
+            return
         if fp8:
             pkv.paged_decode_attention_fp8(q, kc, vc, bt, cl, batch.scale, k_scale, v_scale, H,
                                            Hk, D, bs, max_context_len=mcl, out=out,
@@ -485,9 +510,10 @@ def run_ours(args):
 
     peak, peak_src = load_peak()
     achieved = nbytes["attention"] / (attn_ms_mean * 1e-3) / 1e9
-    traffic = None if fp8 else ncu_traffic(args.workload)  # the summary covers the fp16 kernel
+    # the committed summary covers the fp16 one-token kernel
+    traffic = None if (fp8 or multi) else ncu_traffic(args.workload)
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not fp8:
+    if rank == 0 and not args.no_cpu_baseline and not fp8 and not multi:
         cpu = cpu_baseline(batch, args.cpu_seconds)
 
     if rank != 0:
@@ -511,6 +537,7 @@ def run_ours(args):
                                             "auto (tensor-core kernel when block_size % 16 == 0)"),
             "prefix_shared": groups is not None,
             "kv_dtype": "e4m3 (per-tensor scales)" if fp8 else "f16",
+            "q_len": nq,
         },
         "steps_per_sec": round(1e3 / step_ms, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
