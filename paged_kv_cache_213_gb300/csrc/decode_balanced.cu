@@ -47,6 +47,10 @@ constexpr int kThreadsB = kW * 32;
 constexpr int kMaxSeqsBalanced = 2048;
 constexpr int kMaxWorkers = 16384;  // size of the counter region
 constexpr int kMinUnits = 4;        // fewest units a working warp takes
+// In the suffix pass of the prefix-aware call the private parts are short
+// (forked completions: a block or two), and each output waits for the shared
+// pass; one short segment per warp spreads those fold-ins over more warps.
+constexpr int kMinUnitsSuffix = 2;
 constexpr float kLn2b = 0.69314718055994531f;
 
 template <int D, int G, bool F8>
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(kThreadsB)
     const int w = blockIdx.x * kW + warp;
     const int T = Hk * s_pre[B];
     // at least kMinUnits units per warp: short segments then stay whole
-    const int U = max(kMinUnits, (T + workers - 1) / workers);
+    const int U = max(a.num_groups > 0 ? kMinUnitsSuffix : kMinUnits, (T + workers - 1) / workers);
     const int w0 = static_cast<int>(min(static_cast<long long>(T), static_cast<long long>(w) * U));
     const int n = min(T, w0 + U) - w0;
     if (n <= 0) return;  // no CTA-wide barriers below
