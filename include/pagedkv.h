@@ -170,6 +170,26 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int32_t *err_word, void *cuda_stream);
 
 /*
+ * One decode step in one call: paged_kv_append of num_tokens new tokens, then
+ * paged_decode_attention, on cuda_stream.  Same arguments, results and errors
+ * as the two calls in sequence (the attention's arguments are checked first,
+ * so a rejected call writes nothing).  Because the kernel before the
+ * attention is then known to write only the caches, the attention's prologue
+ * (context lengths, block-table reads, work split) runs while the append
+ * drains, and only its first K/V load waits for the append (programmatic
+ * dependent launch).  The pages have no separate call for this; section 5.1
+ * of "Distributed LLM Inference Serving Platform" describes the two steps of
+ * one decode iteration.
+ */
+int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                      int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                      int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
+                      int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                      int partition_tokens, void *workspace, size_t workspace_bytes,
+                      float *lse_out, int32_t *err_word, void *cuda_stream);
+
+/*
  * Prefix-aware (cascade) decode attention ("Distributed LLM Inference Serving
  * Platform", section 2 and Lab 1: prompt blocks shared by parallel
  * completions; section 5.1 Ingestion: a cached common prefix referenced by

@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     paged_decode_attention_prefix_shared,
     paged_kv_append,
     paged_kv_append_fp8,
+    paged_decode_step,
     prefix_shared_plan,
     status_string,
 )

@@ -507,3 +507,52 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
                 _ptr(lse), _ptr(err_word), _stream_handle(dev))
     _check("paged_decode_attention_multi", rc)
     return out
+
+
+def paged_decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                      context_lens, scale, n_q_heads, n_kv_heads, head_dim, block_size,
+                      max_context_len=None, partition_tokens=0, out=None, workspace=None,
+                      lse=None, err_word=None):
+    """paged_kv_append then paged_decode_attention in one call: the attention's
+    prologue overlaps the append.  Returns out [B, H, d] fp16."""
+    lib = library()
+    fn = lib.paged_decode_step
+    c = ctypes
+    p = c.c_void_p
+    fn.argtypes = [p, p, p, c.c_int, p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float,
+                   c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p, p]
+    fn.restype = c.c_int
+    dev = q.device
+    for t, name, dt in ((k_new, "k_new", torch.float16), (v_new, "v_new", torch.float16),
+                        (slot_mapping, "slot_mapping", torch.int64), (q, "q", torch.float16),
+                        (k_cache, "k_cache", torch.float16), (v_cache, "v_cache", torch.float16),
+                        (block_tables, "block_tables", torch.int32),
+                        (context_lens, "context_lens", torch.int32)):
+        _need(t, name, dt, dev)
+    B, MB = block_tables.shape
+    T = k_new.shape[0]
+    if slot_mapping.shape != (T,) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new [T, Hk, d], slot_mapping [T]")
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    P, ws = decode_plan(B, n_q_heads, n_kv_heads, head_dim, block_size, MB, mcl, partition_tokens)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, dev)
+    if ws > 0:
+        if workspace is None:
+            # zero-filled: the balanced split keeps arrival counters in it
+            workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(out), _ptr(q),
+                _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, MB,
+                k_cache.shape[0], float(scale), n_q_heads, n_kv_heads, head_dim, block_size, mcl,
+                P, _ptr(workspace) if ws > 0 else None, workspace.numel() if ws > 0 else 0,
+                _ptr(lse), _ptr(err_word), _stream_handle(dev))
+    _check("paged_decode_step", rc)
+    return out

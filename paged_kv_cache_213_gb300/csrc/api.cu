@@ -148,6 +148,23 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
     return PKV_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// paged_decode_attention; defer = 2 when this library's append was launched
+// just before on the same stream (the prologue may then run under it).
+int decode_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                          int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
+                          int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                          int partition_tokens, void *workspace, size_t workspace_bytes,
+                          float *lse_out, int32_t *err_word, void *cuda_stream, int defer);
+
+}  // namespace
+
+extern "C" {
+
 int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *block_tables, const int32_t *context_lens,
                            int num_seqs, int max_blocks_per_seq, int64_t num_blocks, float scale,
@@ -155,6 +172,47 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int max_context_len, int partition_tokens, void *workspace,
                            size_t workspace_bytes, float *lse_out, int32_t *err_word,
                            void *cuda_stream) {
+    return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                 max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
+                                 head_dim, block_size, max_context_len, partition_tokens,
+                                 workspace, workspace_bytes, lse_out, err_word, cuda_stream, 0);
+}
+
+int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                      int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                      int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
+                      int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                      int partition_tokens, void *workspace, size_t workspace_bytes,
+                      float *lse_out, int32_t *err_word, void *cuda_stream) {
+    // check the attention's arguments first so that a rejected call changes nothing
+    Plan plan{};
+    int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                       max_context_len, partition_tokens, &plan);
+    if (rc != PKV_OK) return rc;
+    if (num_seqs > 0 && plan.ws_bytes > 0 &&
+        (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)))
+        return PKV_ERR_WORKSPACE;
+    rc = paged_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens, n_kv_heads,
+                         head_dim, block_size, num_blocks, err_word, cuda_stream);
+    if (rc != PKV_OK) return rc;
+    return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                 max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
+                                 head_dim, block_size, max_context_len, partition_tokens,
+                                 workspace, workspace_bytes, lse_out, err_word, cuda_stream,
+                                 num_tokens > 0 ? 2 : 0);
+}
+
+}  // extern "C"
+
+namespace {
+
+int decode_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                          int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
+                          int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                          int partition_tokens, void *workspace, size_t workspace_bytes,
+                          float *lse_out, int32_t *err_word, void *cuda_stream, int defer) {
     if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     Plan plan{};
     int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
@@ -201,6 +259,7 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
     a.max_context_len = plan.max_len;
     a.partition_tokens = plan.partition;
     a.max_parts = plan.max_parts;
+    a.defer_dep_wait = plan.balanced ? defer : 0;
     if (plan.balanced &&
         static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
         return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
@@ -211,6 +270,10 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
 
 // ---------------------------------------------------------------------------
 // FP8 (E4M3) KV caches

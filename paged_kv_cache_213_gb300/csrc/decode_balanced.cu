@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kThreadsB)
         advance(pc, s_pre, B);
     };
 
+    if (a.defer_dep_wait == 2) grid_dependency_wait();  // the append has written the caches
     const int pro = n < kS ? n : kS;
     for (int k = 0; k < pro; ++k) issue(k);
     int issued = pro;

@@ -78,10 +78,15 @@ struct DecodeArgs {
     float *sh_acc;                // [B][H][sh_parts][D] shared-pass partial sums
     float *sh_m;                  // [B][H][sh_parts]
     float *sh_l;                  // [B][H][sh_parts]
-    // 1: the kernel before this one in the stream (the shared-prefix pass)
-    // writes only sh_acc / sh_m / sh_l, so the balanced kernel may run its
-    // prologue and private tiles before its grid-dependency wait and waits
-    // only before it reads those partials.  0: wait first.
+    // Where the balanced kernel waits for the kernel before it in the stream
+    // (programmatic dependent launch):
+    //  0: first thing;
+    //  1: the kernel before is the shared-prefix pass, which writes only
+    //     sh_acc / sh_m / sh_l: prologue and private tiles run before the
+    //     wait, which comes before the first read of those partials;
+    //  2: the kernel before is this library's append, which writes only the
+    //     caches: the prologue (lengths, block ids) runs before the wait,
+    //     which comes before the first K/V load.
     int defer_dep_wait;
     // FP8 caches (balanced kernel only): k_cache / v_cache hold E4M3 codes,
     // scale_log2 already includes k_scale, and outputs are multiplied by v_scale

@@ -309,3 +309,26 @@ def test_balanced_workspace_reuse_across_plans():
             assert_close(out.cpu().numpy(), ref["out"], what=f"{bt.name} rep {rep}")
     counters = work[: 16384 * 4].view(torch.int32)
     assert int(counters.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_decode_step_matches_append_then_attend(cfg):
+    """paged_decode_step (append, then attention whose prologue overlaps it)
+    gives the caches and outputs of the two calls, and matches the oracle."""
+    batch = wl.workload(cfg, poison=True)
+    dev = to_dev(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lse = torch.zeros(batch.num_seqs, batch.n_q_heads, device="cuda")
+    out = pkv.paged_decode_step(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["q"],
+                                dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                dev["context_lens"], batch.scale, batch.n_q_heads,
+                                batch.n_kv_heads, batch.head_dim, batch.block_size,
+                                max_context_len=batch.max_context_len, lse=lse, err_word=err)
+    assert pkv.get_error(err) == 0
+    two = gpu_step(batch)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), two["out"].view(np.uint16))
+    assert np.array_equal(dev["k_cache"].cpu().numpy().view(np.uint16),
+                          two["dev"]["k_cache"].cpu().numpy().view(np.uint16))
+    ref = oracle_step(batch)
+    assert_close(out.cpu().numpy(), ref["out"], what=f"step {cfg}")
+    assert np.max(np.abs(lse.cpu().numpy() - ref["lse"])) <= 1e-4
