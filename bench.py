@@ -553,15 +553,19 @@ def run_ours(args):
         "attention_ms": round(attn_ms_mean, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode_attention (partition kernel + LSE merge)",
+                     "kernel": "paged_decode_attention: decode_balanced_kernel (one launch, "
+                               "in-kernel LSE merge)" if P == 0 else
+                               "paged_decode_attention: partition kernel + LSE merge kernel",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
-        "gpu_launches_note": "append + decode partition + LSE merge per step (merge only when "
-                             "the plan splits); the attention-only timing pass adds "
-                             f"{(launches_per_step - (1 if has_append else 0)) * args.steps} more",
+        "gpu_launches_note": "per step: the append (when the step has one) and the attention "
+                             "kernel(s) -- one balanced kernel, or partition + merge kernels, or "
+                             "the shared-prefix pass + suffix pass; the attention-only timing "
+                             f"pass adds {(launches_per_step - (1 if has_append else 0)) * args.steps}"
+                             " more",
         "clocks": clocks,
         "wall_s_timed": round(wall1 - wall0, 3),
     }
