@@ -424,7 +424,10 @@ int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, 
     // one wave of CTAs over the (group chunk, KV head) pairs, at least 4 tiles each
     const long long pairs =
         static_cast<long long>(num_groups > 0 ? num_groups : 1) * sp->chunks * n_kv_heads;
-    long long parts = (static_cast<long long>(per_sm) * sms) / pairs;
+#ifndef PKV_SHARED_WAVES
+#define PKV_SHARED_WAVES 1
+#endif
+    long long parts = (static_cast<long long>(PKV_SHARED_WAVES) * per_sm * sms) / pairs;
     const long long max_parts = max_tiles > 4 ? max_tiles / 4 : 1;
     if (parts > max_parts) parts = max_parts;
     if (parts < 1) parts = 1;
