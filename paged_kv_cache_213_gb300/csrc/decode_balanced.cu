@@ -426,9 +426,12 @@ __global__ void __launch_bounds__(kThreadsB)
         const int x0 = pj * s_pre[B] + s_pre[pb];  // the segment's units [x0, x0 + nt)
         const int wf = x0 / U;
         const int wl = (x0 + nt - 1) / U;
+        // lane 1 counts: lane 0 issues the ring's TMA loads, and a release by
+        // the lane that issued them could wait for them to land
         int old = 0;
-        if (lane == 0) old = atomic_add_acq_rel_gpu(&counters[wf], 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
+        if (lane == 1) old = atomic_add_acq_rel_gpu(&counters[wf], 1);
+        old = __shfl_sync(0xffffffffu, old, 1);
+        __syncwarp();  // lane 1's acquire before lane 0's bulk copies of the records
         ++piece_no;
         if (old == wl - wf) {  // arrived last: merge later, when the ring is idle
             pend_b[pend_n] = pb;
