@@ -558,12 +558,13 @@ int make_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads, int
     int P = partition_tokens;
     if (P == 0) {
         // the largest power of two in [64, 2048] whose grid still has about
-        // eight warps per SM
+        // eight CTAs per SM (a CTA serves up to four row blocks)
         int sms = 0;
         const int rc = sm_count(&sms);
         if (rc != PKV_OK) return rc;
         P = 2048;
-        const long long items = static_cast<long long>(num_seqs) * n_kv_heads * mp->row_blocks;
+        const int groups = (mp->row_blocks + 3) / 4;
+        const long long items = static_cast<long long>(num_seqs) * n_kv_heads * groups;
         while (P > 64 && items * ((max_len + P - 1) / P) < 8LL * sms) P /= 2;
     } else if (P < 16 || P % 16 != 0 || P % block_size != 0) {
         return PKV_ERR_INVALID_ARG;

@@ -10,13 +10,15 @@
 // query_start[b+1]) of q: its last n_b cached tokens, so query token i sits at
 // position L_b - n_b + i and attends the tokens [0, L_b - n_b + i].
 //
-// Work: one warp per (sequence b, KV head j, block of 16 query rows, KV
-// partition).  The 16 rows of a block are (query token, head) pairs -- row
-// R = i * G + h of the sequence's n_b * G rows for KV head j -- and form the
-// M dimension of mma.m16n8k16; each row has its own causal limit.  K/V tiles
-// of 16 tokens arrive by TMA into a 4-stage ring.  One partition writes the
-// output directly; several write partial (m, l, acc) states that a second
-// kernel merges by log-sum-exp.
+// Work: one CTA per (sequence b, KV head j, group of up to 4 blocks of 16
+// query rows, KV partition), one warp per row block.  The 16 rows of a block
+// are (query token, head) pairs -- row R = i * G + h of the sequence's
+// n_b * G rows for KV head j -- and form the M dimension of mma.m16n8k16;
+// each row has its own causal limit.  K/V tiles of 16 tokens arrive by TMA
+// into a 4-stage ring that every warp of the CTA reads, so a tile is fetched
+// once per group of row blocks.  One partition writes the output directly;
+// several write partial (m, l, acc) states that a second kernel merges by
+// log-sum-exp.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -40,11 +42,13 @@ struct MultiCfg : MmaCfg<D> {
     static constexpr int SMEM = 1024 + kStagesM * STAGE_BYTES;
 };
 
+constexpr int kMaxMultiWarps = 4;
+
 template <int D, int G>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32 * kMaxMultiWarps)
     decode_multi_kernel(const __grid_constant__ DecodeArgs a,
                         const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v, int row_blocks) {
+                        const __grid_constant__ CUtensorMap tmap_v, int row_groups) {
     using C = MultiCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kStagesM];
@@ -52,12 +56,16 @@ __global__ void __launch_bounds__(32)
     const uint32_t raw_s = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
 
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int nwarps = blockDim.x >> 5;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int g = lane >> 2;
     const int tq = lane & 3;
     const int part = blockIdx.x;
-    const int j = blockIdx.y / row_blocks;
-    const int rb = blockIdx.y % row_blocks;
+    const int j = blockIdx.y / row_groups;
+    const int rg = blockIdx.y % row_groups;  // this CTA's group of row blocks
+    const int rb = rg * nwarps + warp;       // this warp's row block
     const int b = blockIdx.z;
     const int H = a.n_q_heads;
     const int Hk = a.n_kv_heads;
@@ -70,11 +78,13 @@ __global__ void __launch_bounds__(32)
     const long long cap_ll = static_cast<long long>(a.max_blocks_per_seq) * bs;
     const int cap = static_cast<int>(cap_ll < a.max_context_len ? cap_ll : a.max_context_len);
     if (L < 0 || L > cap || n < 0 || n > L || q0 < 0 || q0 + n > a.total_q) {
-        if (lane == 0 && part == 0 && blockIdx.y == 0) flag_error(a.err, PKV_ERRBIT_CONTEXT);
+        if (tid == 0 && part == 0 && blockIdx.y == 0) flag_error(a.err, PKV_ERRBIT_CONTEXT);
         return;
     }
+    const int nrb = (n * G + 15) / 16;  // row blocks of this sequence
+    if (rg * nwarps >= nrb) return;      // no query rows in this CTA (uniform)
+    const bool warp_rows = rb < nrb;     // warps past the last block only help with barriers
     const int R0 = rb * 16;
-    if (R0 >= n * G) return;  // no query rows in this block
     // query rows of this lane: r_lo = R0 + g, r_hi = R0 + g + 8
     const int r_lo = R0 + g, r_hi = R0 + g + 8;
     const bool has_lo = r_lo < n * G, has_hi = r_hi < n * G;
@@ -83,12 +93,14 @@ __global__ void __launch_bounds__(32)
     // causal limits (exclusive) in absolute token positions
     const int lim_lo = has_lo ? L - n + i_lo + 1 : 0;
     const int lim_hi = has_hi ? L - n + i_hi + 1 : 0;
-    const int i_last = min(n - 1, (R0 + 15) / G);
-    const int end = L - n + i_last + 1;  // tokens any row of the block needs
+    // tokens any row of the CTA needs: up to its last query token
+    const int rb_last = min(nrb - 1, rg * nwarps + nwarps - 1);
+    const int i_last = min(n - 1, (rb_last * 16 + 15) / G);
+    const int end = L - n + i_last + 1;
     const int P = a.partition_tokens;
     const int t_begin = part * P;
     const int t_end = min(end, t_begin + P);
-    if (t_begin >= end) return;  // no row of the block reads this partition
+    if (t_begin >= end) return;  // no row of the CTA reads this partition (uniform)
     const int ntiles = (t_end - t_begin + kMmaTile - 1) / kMmaTile;
 
     const __half *qb = static_cast<const __half *>(a.q);
@@ -99,7 +111,7 @@ __global__ void __launch_bounds__(32)
                    has_hi, tq);
 
     const int32_t *bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks_per_seq;
-    auto issue = [&](int k) {  // lane 0
+    auto issue = [&](int k) {  // thread 0
         const int st = k % kStagesM;
         const int tok0 = t_begin + k * kMmaTile;
         const int id = bt[tok0 / bs];
@@ -118,14 +130,14 @@ __global__ void __launch_bounds__(32)
             }
         }
     };
-    if (lane == 0) {
+    if (tid == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
         for (int s = 0; s < kStagesM; ++s) mbar_init(&full_bar[s], 1);
         fence_barrier_init();
         for (int k = 0; k < ntiles && k < kStagesM; ++k) issue(k);
     }
-    __syncwarp();
+    __syncthreads();
 
     float o[C::NB_D][4];
 #pragma unroll
@@ -135,8 +147,8 @@ __global__ void __launch_bounds__(32)
     for (; k < ntiles; ++k) {
         const int st = k % kStagesM;
         const bool ok = mbar_wait_bounded(&full_bar[st], (k / kStagesM) & 1);
-        if (__any_sync(0xffffffffu, !ok)) break;
-        if (s_ok[st]) {
+        if (__syncthreads_or(!ok)) break;
+        if (warp_rows && s_ok[st]) {
             const int tok0 = t_begin + k * kMmaTile;
             unsigned char *ks = smem + st * C::STAGE_BYTES;
             mma_tile_multi<D>(ks, ks + C::TILE_BYTES, min(kMmaTile, L - tok0),
@@ -144,11 +156,11 @@ __global__ void __launch_bounds__(32)
                               max(0, min(kMmaTile, lim_hi - tok0)), qlo, qhi, a.scale_log2, o,
                               m_lo, l_lo, m_hi, l_hi, lane);
         }
-        __syncwarp();
-        if (lane == 0 && k + kStagesM < ntiles) issue(k + kStagesM);
+        __syncthreads();  // every warp is done with stage st
+        if (tid == 0 && k + kStagesM < ntiles) issue(k + kStagesM);
     }
     if (k < ntiles) {  // a copy never arrived: flag, drain what is in flight
-        if (lane == 0) {
+        if (tid == 0) {
             flag_error(a.err, PKV_ERRBIT_TIMEOUT);
             for (int kk = k; kk < ntiles && kk < k + kStagesM; ++kk)
                 mbar_wait_bounded(&full_bar[kk % kStagesM], (kk / kStagesM) & 1);
@@ -181,6 +193,7 @@ __global__ void __launch_bounds__(32)
             a.ws_l[r] = l;
         }
     };
+    if (!warp_rows) return;
     emit(has_lo, i_lo, h_lo, m_lo, l_lo, 0);
     emit(has_hi, i_hi, h_hi, m_hi, l_hi, 2);
 }
@@ -239,10 +252,14 @@ cudaError_t launch_multi_t(const DecodeArgs &a, int row_blocks, const CUtensorMa
     const int smem = MultiCfg<D>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long y = static_cast<long long>(a.n_kv_heads) * row_blocks;
+    // one warp per row block, up to kMaxMultiWarps row blocks per CTA
+    const int nw = row_blocks < kMaxMultiWarps ? row_blocks : kMaxMultiWarps;
+    const int row_groups = (row_blocks + nw - 1) / nw;
+    const long long y = static_cast<long long>(a.n_kv_heads) * row_groups;
     if (y > 65535 || a.num_seqs > 65535) return cudaErrorInvalidValue;
     dim3 grid(a.max_parts, static_cast<unsigned>(y), a.num_seqs);
-    e = launch_pdl(kern, grid, dim3(32), static_cast<size_t>(smem), stream, a, tk, tv, row_blocks);
+    e = launch_pdl(kern, grid, dim3(32 * nw), static_cast<size_t>(smem), stream, a, tk, tv,
+                   row_groups);
     if (e != cudaSuccess || a.max_parts == 1) return e;
     const long long warps = static_cast<long long>(a.total_q) * a.n_q_heads;
     const long long blocks = (warps * 32 + 255) / 256;
