@@ -391,18 +391,35 @@ def run_ours(args):
             attend()
 
     # host-pinned copies of the per-step inputs for the end-to-end leg
-    pin = {}
+    # The per-step inputs live as 256-byte-aligned views of one device buffer,
+    # mirrored by one pinned host buffer: the end-to-end leg moves them with a
+    # single host-to-device copy per step.
+    stage_host = stage_dev = None
     if not args.no_e2e:
-        for name, a in (("q", q), ("bt", bt), ("cl", cl)) + \
-                ((("kn", kn), ("vn", vn), ("sm", sm)) if has_append else ()):
-            pin[name] = (a.cpu().pin_memory(), a)
+        names = [("q", q), ("bt", bt), ("cl", cl)] + \
+            ([("kn", kn), ("vn", vn), ("sm", sm)] if has_append else [])
+        offs, total = [], 0
+        for _, a in names:
+            offs.append(total)
+            total += (a.numel() * a.element_size() + 255) // 256 * 256
+        stage_dev = torch.zeros(total, dtype=torch.uint8, device=device)
+        stage_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        views = {}
+        for (name, a), off in zip(names, offs):
+            nb = a.numel() * a.element_size()
+            v = stage_dev[off:off + nb].view(a.dtype).view(a.shape)
+            v.copy_(a)
+            stage_host[off:off + nb].copy_(a.cpu().contiguous().view(-1).view(torch.uint8))
+            views[name] = v
+        q, bt, cl = views["q"], views["bt"], views["cl"]
+        if has_append:
+            kn, vn, sm = views["kn"], views["vn"], views["sm"]
         out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d_bytes = sum(h.numel() * h.element_size() for h, _ in pin.values())
+        h2d_bytes = total
         d2h_bytes = out_host.numel() * out_host.element_size()
 
     def e2e_inputs():
-        for h, d in pin.values():
-            d.copy_(h, non_blocking=True)
+        stage_dev.copy_(stage_host, non_blocking=True)
 
     # eager warm-up (also sets kernel attributes before any capture)
     for _ in range(max(3, args.warmup)):
