@@ -181,6 +181,18 @@ __global__ void __launch_bounds__(kThreadsB)
     const int bs = a.block_size;
     char *ws = reinterpret_cast<char *>(a.ws_acc);
     int *counters = reinterpret_cast<int *>(ws);
+    // barriers and tensor-map prefetch first: they overlap the loads below
+    if (tid == 0) {
+        if constexpr (!F8) {  // E4M3 tiles use plain bulk copies, no tensor map
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
+        for (int w = 0; w < kW; ++w) {
+            for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
+            mbar_init(&merge_bar[w], 1);
+        }
+        fence_barrier_init();
+    }
     // the previous kernel in the stream (e.g. the append) is done; after the
     // shared-prefix pass, only the reads of its partials have to wait
     if (!a.defer_dep_wait) grid_dependency_wait();
@@ -216,17 +228,6 @@ __global__ void __launch_bounds__(kThreadsB)
         if (lane >= off) incl += v;
     }
     if (lane == 31) s_scan[warp] = incl;
-    if (tid == 0) {
-        if constexpr (!F8) {  // E4M3 tiles use plain bulk copies, no tensor map
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
-        for (int w = 0; w < kW; ++w) {
-            for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
-            mbar_init(&merge_bar[w], 1);
-        }
-        fence_barrier_init();
-    }
     __syncthreads();
     int base = 0;
     for (int w = 0; w < warp; ++w) base += s_scan[w];
