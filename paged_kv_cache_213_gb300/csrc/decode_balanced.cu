@@ -635,6 +635,15 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
 #undef PKV_BAL_OCC
     const int sms = sm_count_cached();
     if (per_sm <= 0 || sms <= 0) return false;
+    // Few (sequence, KV head) segments: each is long and every warp range
+    // lies inside one, so more warps only cut the segments into more pieces
+    // (more records, release fences and merges).  Two CTAs per SM then beat
+    // three (LLaMA-3-8B-shaped layer, 256 segments: 44.6 -> 41.5 us; 32k
+    // contexts, 64 segments: 187 -> 180 us).  Many short segments are seldom
+    // cut and gain from the extra warps (Mistral mix, 1024 segments: 45 ->
+    // 53 us at two), and so does the E4M3 path, which is issue-bound.
+    if (!kv_fp8 && static_cast<long long>(num_seqs) * n_kv_heads <= 2LL * sms && per_sm > 2)
+        per_sm = 2;
     // units must fit 32-bit arithmetic: Hk * B * tiles per sequence
     const long long t_max = static_cast<long long>(n_kv_heads) * num_seqs *
                             ((static_cast<long long>(max_len) + kMmaTile - 1) / kMmaTile);
