@@ -38,12 +38,14 @@
 namespace pkv {
 namespace {
 
-constexpr int kW = 4;  // warps per CTA, each an independent worker
+// Warps per CTA (each an independent worker): 4, three CTAs per SM; or 8,
+// one CTA per SM, for batches of few long segments (balanced_plan).
+constexpr int kWSmall = 4;
+constexpr int kWLarge = 8;
 #ifndef PKV_BAL_STAGES
 #define PKV_BAL_STAGES 2
 #endif
 constexpr int kS = PKV_BAL_STAGES;  // ring stages per warp
-constexpr int kThreadsB = kW * 32;
 constexpr int kMaxSeqsBalanced = 2048;
 constexpr int kMaxWorkers = 16384;  // size of the counter region
 constexpr int kMinUnits = 4;        // fewest units a working warp takes
@@ -53,7 +55,7 @@ constexpr int kMinUnits = 4;        // fewest units a working warp takes
 constexpr int kMinUnitsSuffix = 2;
 constexpr float kLn2b = 0.69314718055994531f;
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int kW>
 struct BalCfg : MmaCfg<D> {
     static constexpr int Q_BYTES = G * D * 2;  // the group's query rows
     // one tile of one cache in the ring: fp16 (TMA boxes) or E4M3 bytes
@@ -152,12 +154,13 @@ __device__ __forceinline__ void advance(Cursor &c, const int *pre, int B) {
     while (c.b < B && pre[c.b + 1] == pre[c.b]) ++c.b;
 }
 
-template <int D, int G, bool F8>
-__global__ void __launch_bounds__(kThreadsB)
+template <int D, int G, bool F8, int kW>
+__global__ void __launch_bounds__(kW * 32)
     decode_balanced_kernel(const __grid_constant__ DecodeArgs a,
                            const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const int workers) {
-    using C = BalCfg<D, G, F8>;
+    using C = BalCfg<D, G, F8, kW>;
+    constexpr int kThreadsB = kW * 32;
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kW][kS];
     __shared__ uint64_t merge_bar[kW];
@@ -558,41 +561,42 @@ __global__ void __launch_bounds__(kThreadsB)
     }
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int kW>
 size_t bal_smem(int B) {
-    using C = BalCfg<D, G, F8>;
+    using C = BalCfg<D, G, F8, kW>;
     return 1024 + C::PIPE_BYTES + C::QS_BYTES + (3 * static_cast<size_t>(B) + 1) * 4;
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int kW>
 int bal_ctas_per_sm(int B) {
     static std::mutex mu;
     static std::map<size_t, int> cache;
-    const size_t smem = bal_smem<D, G, F8>(B);
+    const size_t smem = bal_smem<D, G, F8, kW>(B);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(smem);
     if (it != cache.end()) return it->second;
-    auto kern = decode_balanced_kernel<D, G, F8>;
+    auto kern = decode_balanced_kernel<D, G, F8, kW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(bal_smem<D, G, F8>(kMaxSeqsBalanced))) != cudaSuccess)
+                             static_cast<int>(bal_smem<D, G, F8, kW>(kMaxSeqsBalanced))) !=
+        cudaSuccess)
         return 0;
     // the grid is sized to fill every SM once: ask for the whole carve-out
     if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreadsB, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kW * 32, smem) != cudaSuccess)
         return 0;
     cache[smem] = n;
     return n;
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int kW>
 cudaError_t launch_bal_t(const DecodeArgs &a, const BalancedPlan &plan, const CUtensorMap &tk,
                          const CUtensorMap &tv, cudaStream_t stream) {
-    auto kern = decode_balanced_kernel<D, G, F8>;
-    if (bal_ctas_per_sm<D, G, F8>(a.num_seqs) <= 0) return cudaErrorInvalidConfiguration;
-    return launch_pdl(kern, dim3(plan.ctas), dim3(kThreadsB), bal_smem<D, G, F8>(a.num_seqs),
+    auto kern = decode_balanced_kernel<D, G, F8, kW>;
+    if (bal_ctas_per_sm<D, G, F8, kW>(a.num_seqs) <= 0) return cudaErrorInvalidConfiguration;
+    return launch_pdl(kern, dim3(plan.ctas), dim3(kW * 32), bal_smem<D, G, F8, kW>(a.num_seqs),
                       stream, a, tk, tv, plan.workers);
 }
 
@@ -619,11 +623,24 @@ bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
 bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
                    BalancedPlan *plan, bool kv_fp8) {
     const int G = n_q_heads / n_kv_heads;
+    const int sms = sm_count_cached();
+    if (sms <= 0) return false;
+    // Few (sequence, KV head) segments: each is long and every warp range
+    // lies inside one, so more warps only cut the segments into more pieces
+    // (more records, release fences and merges).  Eight warps per SM, as one
+    // CTA, then beat twelve (LLaMA-3-8B-shaped layer, 256 segments: 44.5 ->
+    // 40.2 us; 32k contexts, 64 segments: 187 -> 175 us).  Many short
+    // segments are seldom cut and gain from the extra warps (Mistral mix,
+    // 1024 segments: 45 -> 53 us at eight), and so does the E4M3 path, which
+    // is issue-bound.
+    const bool few = !kv_fp8 && static_cast<long long>(num_seqs) * n_kv_heads <= 2LL * sms;
+    const int warps = few ? kWLarge : kWSmall;
     int per_sm = 0;
 #define PKV_BAL_OCC(D_, G_)                                                               \
     if (head_dim == D_ && G == G_)                                                          \
-        per_sm = kv_fp8 ? bal_ctas_per_sm<D_, G_, true>(num_seqs)                          \
-                        : bal_ctas_per_sm<D_, G_, false>(num_seqs);
+        per_sm = kv_fp8 ? bal_ctas_per_sm<D_, G_, true, kWSmall>(num_seqs)                 \
+                        : (few ? bal_ctas_per_sm<D_, G_, false, kWLarge>(num_seqs)         \
+                               : bal_ctas_per_sm<D_, G_, false, kWSmall>(num_seqs));
     PKV_BAL_OCC(128, 1)
     PKV_BAL_OCC(128, 2)
     PKV_BAL_OCC(128, 4)
@@ -633,28 +650,20 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
     PKV_BAL_OCC(64, 4)
     PKV_BAL_OCC(64, 8)
 #undef PKV_BAL_OCC
-    const int sms = sm_count_cached();
-    if (per_sm <= 0 || sms <= 0) return false;
-    // Few (sequence, KV head) segments: each is long and every warp range
-    // lies inside one, so more warps only cut the segments into more pieces
-    // (more records, release fences and merges).  Two CTAs per SM then beat
-    // three (LLaMA-3-8B-shaped layer, 256 segments: 44.6 -> 41.5 us; 32k
-    // contexts, 64 segments: 187 -> 180 us).  Many short segments are seldom
-    // cut and gain from the extra warps (Mistral mix, 1024 segments: 45 ->
-    // 53 us at two), and so does the E4M3 path, which is issue-bound.
-    if (!kv_fp8 && static_cast<long long>(num_seqs) * n_kv_heads <= 2LL * sms && per_sm > 2)
-        per_sm = 2;
+    if (per_sm <= 0) return false;
+    if (few && per_sm * warps > kWLarge) per_sm = kWLarge / warps > 0 ? kWLarge / warps : 1;
     // units must fit 32-bit arithmetic: Hk * B * tiles per sequence
     const long long t_max = static_cast<long long>(n_kv_heads) * num_seqs *
                             ((static_cast<long long>(max_len) + kMmaTile - 1) / kMmaTile);
     if (t_max >= (1LL << 31)) return false;
     long long ctas = static_cast<long long>(sms) * per_sm;
-    const long long need = (t_max + 2 * kW - 1) / (2 * kW);  // >= 2 tiles per warp on average
+    const long long need = (t_max + 2 * warps - 1) / (2 * warps);  // >= 2 tiles per warp on average
     if (need < ctas) ctas = need;
-    if (ctas * kW > kMaxWorkers) ctas = kMaxWorkers / kW;
+    if (ctas * warps > kMaxWorkers) ctas = kMaxWorkers / warps;
     if (ctas < 1) ctas = 1;
     plan->ctas = static_cast<int>(ctas);
-    plan->workers = plan->ctas * kW;
+    plan->warps = warps;
+    plan->workers = plan->ctas * warps;
     plan->ws_bytes = bal_ws_bytes(plan->workers, G, head_dim);
     return true;
 }
@@ -667,10 +676,12 @@ cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan
                       !make_cache_map(&tv, a.v_cache, rows, a.head_dim)))
         return cudaErrorNotSupported;
     const int g = a.n_q_heads / a.n_kv_heads;
-#define PKV_BAL_CASE(D_, G_)                                                       \
-    if (a.head_dim == D_ && g == G_)                                                \
-        return a.kv_fp8 ? launch_bal_t<D_, G_, true>(a, plan, tk, tv, stream)      \
-                        : launch_bal_t<D_, G_, false>(a, plan, tk, tv, stream);
+#define PKV_BAL_CASE(D_, G_)                                                             \
+    if (a.head_dim == D_ && g == G_)                                                      \
+        return a.kv_fp8 ? launch_bal_t<D_, G_, true, kWSmall>(a, plan, tk, tv, stream)   \
+                        : (plan.warps == kWLarge                                          \
+                               ? launch_bal_t<D_, G_, false, kWLarge>(a, plan, tk, tv, stream) \
+                               : launch_bal_t<D_, G_, false, kWSmall>(a, plan, tk, tv, stream));
     PKV_BAL_CASE(128, 1)
     PKV_BAL_CASE(128, 2)
     PKV_BAL_CASE(128, 4)

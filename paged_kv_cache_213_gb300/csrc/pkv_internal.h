@@ -126,7 +126,8 @@ bool make_cache_map(CUtensorMap *m, const void *base, long long rows, int D);
 // Balanced (work-split per warp) tensor-core kernel (decode_balanced.cu).
 struct BalancedPlan {
     int ctas;        // grid size
-    int workers;     // warps doing work = 4 * ctas
+    int warps;       // warps per CTA (4 or 8)
+    int workers;     // warps doing work = warps * ctas
     size_t ws_bytes; // workspace bytes
 };
 bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
