@@ -186,6 +186,18 @@ def workload_bytes(batch, kv_bytes=2):
             "logical_step": s["step_logical"], "stats": s}
 
 
+# decoder layers of the model each workload is shaped like; the whole-model
+# figure (steps/sec divided by layers) is context only: attention alone
+MODEL_LAYERS = {1: 1, 2: 32, 3: 32, 4: 32, 5: 80}
+
+
+def pcts(xs):
+    """p10 / p50 / p90 of a list of times in ms."""
+    ys = sorted(xs)
+    at = lambda f: ys[min(len(ys) - 1, int(round(f * (len(ys) - 1))))]  # noqa: E731
+    return {"p10": round(at(0.1), 5), "p50": round(at(0.5), 5), "p90": round(at(0.9), 5)}
+
+
 def source_sha():
     h = hashlib.sha256()
     for name in ("decode_balanced.cu", "mma_tile.cuh", "pkv_ptx.cuh", "shared_prefix.cuh"):
@@ -470,10 +482,11 @@ def run_ours(args):
         ev[1].record()
     e2e_body.n_events = 2
 
-    def timed(body, steps):
-        """Per-step device times (ms) of each event interval over `steps` steps."""
+    def timed(body, steps, eager=False):
+        """Per-step device times (ms) of each event interval over `steps` steps:
+        inside CUDA-graph replays, or around eager launches when `eager`."""
         intervals = [[] for _ in range(body.n_events - 1)]
-        if in_graph_events:
+        if in_graph_events and not eager:
             g, evs = capture(body)
             g.replay()  # one untimed replay after capture
             torch.cuda.synchronize()
@@ -526,6 +539,10 @@ def run_ours(args):
     attn_ms_mean = statistics.fmean(attn_ms)
     step_ms, value = aggregate(step_ms_rank, nbytes["step"] / 1e9, world, device)
 
+    # one eager-launch figure for the same step (host launch gaps included)
+    eager_steps = min(args.steps, 200)
+    (eager_ms,) = timed(step_body, eager_steps, eager=True)
+
     e2e = None
     if not args.no_e2e:
         (e2e_ms_list,) = timed(e2e_body, args.steps)
@@ -534,6 +551,7 @@ def run_ours(args):
         e2e = {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
                "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(e2e_ms, 5)}
 
+    layers = MODEL_LAYERS.get(args.workload, 1)
     peak, peak_src = load_peak()
     achieved = nbytes["attention"] / (attn_ms_mean * 1e-3) / 1e9
     # the committed summary covers the fp16 one-token kernel
@@ -568,6 +586,10 @@ def run_ours(args):
         "steps_per_sec": round(1e3 / step_ms, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "attention_ms": round(attn_ms_mean, 5),
+        "percentiles_ms": {"step": pcts(step_ms_list), "attention": pcts(attn_ms)},
+        "eager_step_ms": round(statistics.fmean(eager_ms), 5),
+        "model_context": {"layers": layers,
+                          "model_steps_per_sec": round(1e3 / step_ms / layers, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "paged_decode_attention: decode_balanced_kernel (one launch, "
@@ -582,7 +604,7 @@ def run_ours(args):
                              "kernel(s) -- one balanced kernel, or partition + merge kernels, or "
                              "the shared-prefix pass + suffix pass; the attention-only timing "
                              f"pass adds {(launches_per_step - (1 if has_append else 0)) * args.steps}"
-                             " more",
+                             f" more, the eager pass {launches_per_step * eager_steps} more",
         "clocks": clocks,
         "wall_s_timed": round(wall1 - wall0, 3),
     }

@@ -50,3 +50,12 @@ def test_single_process_is_identity():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.aggregate(2.0, 0.5, 1) == (2.0, pytest.approx(250.0))
+
+
+def test_percentiles_of_step_times():
+    sys.path.insert(0, ROOT)
+    import bench
+    xs = [float(v) for v in range(100, 0, -1)]   # 1 .. 100 ms, unsorted
+    p = bench.pcts(xs)
+    assert p == {"p10": 11.0, "p50": 51.0, "p90": 90.0}
+    assert bench.pcts([7.0]) == {"p10": 7.0, "p50": 7.0, "p90": 7.0}
