@@ -61,8 +61,8 @@ struct BalCfg : MmaCfg<D> {
     // one tile of one cache in the ring: fp16 (TMA boxes) or E4M3 bytes
     static constexpr int KV_BYTES = F8 ? kMmaTile * D : MmaCfg<D>::TILE_BYTES;
     static constexpr int SLOT_BYTES = 2 * KV_BYTES;  // K tile, V tile
-    // FP8: the converted fp16 K and V tiles the tile math reads
-    static constexpr int STAGE_BYTES = F8 ? 2 * MmaCfg<D>::TILE_BYTES : 0;
+    // FP8: the V tile widened to fp16 (the tile math widens K as it reads it)
+    static constexpr int STAGE_BYTES = F8 ? MmaCfg<D>::TILE_BYTES : 0;
     static constexpr int WARP_BYTES = kS * SLOT_BYTES + STAGE_BYTES;  // multiple of 1024
     static constexpr int PIPE_BYTES = kW * WARP_BYTES;
     static constexpr int QS_BYTES = kW * kS * Q_BYTES;
@@ -186,10 +186,8 @@ __global__ void __launch_bounds__(kW * 32)
     int *counters = reinterpret_cast<int *>(ws);
     // barriers and tensor-map prefetch first: they overlap the loads below
     if (tid == 0) {
-        if constexpr (!F8) {  // E4M3 tiles use plain bulk copies, no tensor map
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
+        prefetch_tmap(&tmap_k);
+        if constexpr (!F8) prefetch_tmap(&tmap_v);  // E4M3 V tiles move by bulk copies
         for (int w = 0; w < kW; ++w) {
             for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
             mbar_init(&merge_bar[w], 1);
@@ -320,11 +318,13 @@ __global__ void __launch_bounds__(kW * 32)
                 unsigned char *kdst = my_pipe + slot * C::SLOT_BYTES;
                 unsigned char *vdst = kdst + C::KV_BYTES;
                 const int row = (id * Hk + pc.j) * bs + (tok0 % bs);
-                if constexpr (F8) {  // a tile of E4M3 rows is contiguous: two bulk copies
-                    const size_t off = static_cast<size_t>(row) * D;
-                    bulk_copy_g2s(kdst, static_cast<const unsigned char *>(a.k_cache) + off,
-                                  C::KV_BYTES, bar);
-                    bulk_copy_g2s(vdst, static_cast<const unsigned char *>(a.v_cache) + off,
+                if constexpr (F8) {
+                    // K: one swizzled box, read in place by the tile math; V: the
+                    // tile's rows are contiguous, one bulk copy
+                    tma_load_2d(kdst, &tmap_k, 0, row, bar);
+                    bulk_copy_g2s(vdst,
+                                  static_cast<const unsigned char *>(a.v_cache) +
+                                      static_cast<size_t>(row) * D,
                                   C::KV_BYTES, bar);
                 } else {
 #pragma unroll
@@ -526,16 +526,14 @@ __global__ void __launch_bounds__(kW * 32)
         last_t = cc.t;
         unsigned char *ks = my_pipe + slot * C::SLOT_BYTES;
         unsigned char *vs = ks + C::KV_BYTES;
-        if constexpr (F8) {  // widen the E4M3 tiles into the fp16 layout
-            e4m3_tile_to_f16<D>(ks, my_stage, lane);
-            e4m3_tile_to_f16<D>(vs, my_stage + C::TILE_BYTES, lane);
+        if constexpr (F8) {  // widen the E4M3 V tile into the fp16 layout
+            e4m3_tile_to_f16<D>(vs, my_stage, lane);
             __syncwarp();
-            ks = my_stage;
-            vs = my_stage + C::TILE_BYTES;
+            vs = my_stage;
         }
         const int n_valid =
             s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - (cc.t + s_skip[cc.b]) * kMmaTile) : 0;
-        mma_tile<D>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
+        mma_tile<D, F8>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
         __syncwarp();
         if (k + kS < n) {
             issue(k + kS);
@@ -671,9 +669,10 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
 cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
                                    cudaStream_t stream) {
     const long long rows = a.num_blocks * a.n_kv_heads * static_cast<long long>(a.block_size);
-    CUtensorMap tk{}, tv{};  // FP8 caches move by plain bulk copies, no tensor map
-    if (!a.kv_fp8 && (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
-                      !make_cache_map(&tv, a.v_cache, rows, a.head_dim)))
+    CUtensorMap tk{}, tv{};  // E4M3 V tiles move by plain bulk copies, no tensor map
+    if (a.kv_fp8 ? !make_cache_map_e4m3(&tk, a.k_cache, rows, a.head_dim)
+                 : (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
+                    !make_cache_map(&tv, a.v_cache, rows, a.head_dim)))
         return cudaErrorNotSupported;
     const int g = a.n_q_heads / a.n_kv_heads;
 #define PKV_BAL_CASE(D_, G_)                                                             \

@@ -299,6 +299,20 @@ bool make_cache_map(CUtensorMap *m, const void *base, long long rows, int D) {
     return r == CUDA_SUCCESS;
 }
 
+bool make_cache_map_e4m3(CUtensorMap *m, const void *base, long long rows, int D) {
+    auto fn = encode_fn();
+    if (!fn || (D != 64 && D != 128)) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(D), kTile};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool decode_mma_supported(const DecodeArgs &a) {
     const int g = a.n_q_heads / a.n_kv_heads;
     const long long rows = a.num_blocks * a.n_kv_heads * static_cast<long long>(a.block_size);

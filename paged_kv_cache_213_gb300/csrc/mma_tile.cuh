@@ -16,6 +16,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cmath>
 
@@ -36,6 +37,23 @@ struct MmaCfg {
 
 // Byte offset of 16-byte unit `unit` (0-7) of row `row` in a 128B-swizzled box.
 __device__ __forceinline__ int swz(int row, int unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
+
+// Piece p (as above) of row t of an E4M3 K tile staged by TMA with the D-byte
+// swizzle (D = 128: 128B, 16-byte unit u of row t at u ^ (t & 7); D = 64:
+// 64B, at u ^ ((t >> 1) & 3)), widened to the four fp16 pairs that the same
+// piece of an fp16 tile holds.  Every E4M3 code is exact in fp16.
+template <int D>
+__device__ __forceinline__ uint4 e4m3_piece(const unsigned char *ks, int t, int p, int tq) {
+    const int u = 4 * (p >> 1) + tq;  // 16-byte unit of the piece; it starts 8 * (p & 1) in
+    const int off = D == 128 ? swz(t, u) : t * 64 + ((u ^ ((t >> 1) & 3)) << 4);
+    const uint2 w = *reinterpret_cast<const uint2 *>(ks + off + 8 * (p & 1));
+    auto cvt2 = [](uint32_t two) {  // the low two codes of `two`
+        const __half2_raw h =
+            __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+        return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+    };
+    return make_uint4(cvt2(w.x), cvt2(w.x >> 16), cvt2(w.y), cvt2(w.y >> 16));
+}
 
 // Q fragments of head g from a row-major [.., D] fp16 row (global or shared).
 template <int D>
@@ -59,7 +77,8 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qa)[MmaCfg<D>::NP][4], co
 // One tile: rows [0, n_valid) of the K tile `ks` and V tile `vs` take part;
 // the V rows past n_valid are zeroed first (they may hold another sequence's
 // data or NaN and must not reach P.V).  Updates the running state of head g.
-template <int D>
+// K8: `ks` is an E4M3 K tile (e4m3_piece), widened piece by piece.
+template <int D, bool K8 = false>
 __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char *vs, int n_valid,
                                          const uint32_t (&qa)[MmaCfg<D>::NP][4],
                                          float scale_log2, float (&o)[MmaCfg<D>::NB_D][4],
@@ -87,8 +106,12 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
         const int t = nb * 8 + g;
 #pragma unroll
         for (int p = 0; p < C::NP; ++p) {
-            const uint4 kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
-                                                              swz(t, 2 * tq + (p & 1)));
+            uint4 kw;
+            if constexpr (K8)
+                kw = e4m3_piece<D>(ks, t, p, tq);
+            else
+                kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
+                                                      swz(t, 2 * tq + (p & 1)));
             const uint32_t a0[4] = {qa[p][0], 0u, qa[p][1], 0u};
             mma_16816(sacc[nb], a0, kw.x, kw.y);
             const uint32_t a1[4] = {qa[p][2], 0u, qa[p][3], 0u};

@@ -122,6 +122,9 @@ bool decode_mma_supported(const DecodeArgs &a);
 cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t stream);
 // 2-D TMA map [rows][D] fp16 of a cache, 16x64 boxes, 128-byte swizzle.
 bool make_cache_map(CUtensorMap *m, const void *base, long long rows, int D);
+// The same over an E4M3 cache (one byte per element): one box is a whole
+// 16-row tile, D bytes wide, with the D-byte swizzle (128B or 64B).
+bool make_cache_map_e4m3(CUtensorMap *m, const void *base, long long rows, int D);
 
 // Balanced (work-split per warp) tensor-core kernel (decode_balanced.cu).
 struct BalancedPlan {
