@@ -61,42 +61,10 @@ struct BalCfg : MmaCfg<D> {
     // one tile of one cache in the ring: fp16 (TMA boxes) or E4M3 bytes
     static constexpr int KV_BYTES = F8 ? kMmaTile * D : MmaCfg<D>::TILE_BYTES;
     static constexpr int SLOT_BYTES = 2 * KV_BYTES;  // K tile, V tile
-    // FP8: the V tile widened to fp16 (the tile math widens K as it reads it)
-    static constexpr int STAGE_BYTES = F8 ? MmaCfg<D>::TILE_BYTES : 0;
-    static constexpr int WARP_BYTES = kS * SLOT_BYTES + STAGE_BYTES;  // multiple of 1024
+    static constexpr int WARP_BYTES = kS * SLOT_BYTES;  // multiple of 1024
     static constexpr int PIPE_BYTES = kW * WARP_BYTES;
     static constexpr int QS_BYTES = kW * kS * Q_BYTES;
 };
-
-// E4M3 tile (16 rows x D bytes, row-major) -> the fp16 tile layout that the
-// TMA loads give (D/64 boxes of 16 rows x 128 bytes, 128-byte swizzle).
-// Every code is exact in fp16 (cvt.rn.f16x2.e4m3x2); lane-contiguous reads.
-template <int D>
-__device__ __forceinline__ void e4m3_tile_to_f16(const unsigned char *src, unsigned char *dst,
-                                                 int lane) {
-    constexpr int ROW_UNITS = D / 16;  // 16-byte units of an E4M3 row
-#pragma unroll
-    for (int u = lane; u < kMmaTile * ROW_UNITS; u += 32) {
-        const int row = u / ROW_UNITS;
-        const int col = (u % ROW_UNITS) * 16;  // first of the unit's 16 columns
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + u * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(w[i] & 0xffffu), __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-            h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-            h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-        }
-        unsigned char *box = dst + (col / 64) * MmaCfg<D>::BOX_BYTES;
-        const int unit = (col % 64) / 8;
-        *reinterpret_cast<uint4 *>(box + swz(row, unit)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(box + swz(row, unit + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-    }
-}
 
 // Workspace: int counters[kMaxWorkers] at offset 0 (whatever the plan, so
 // that a workspace reused by another plan still starts zeroed), then one
@@ -187,7 +155,7 @@ __global__ void __launch_bounds__(kW * 32)
     // barriers and tensor-map prefetch first: they overlap the loads below
     if (tid == 0) {
         prefetch_tmap(&tmap_k);
-        if constexpr (!F8) prefetch_tmap(&tmap_v);  // E4M3 V tiles move by bulk copies
+        prefetch_tmap(&tmap_v);
         for (int w = 0; w < kW; ++w) {
             for (int s = 0; s < kS; ++s) mbar_init(&full_bar[w][s], 1);
             mbar_init(&merge_bar[w], 1);
@@ -276,7 +244,6 @@ __global__ void __launch_bounds__(kW * 32)
     if (n <= 0) return;  // no CTA-wide barriers below
 
     unsigned char *my_pipe = smem + warp * C::WARP_BYTES;
-    unsigned char *my_stage = my_pipe + kS * C::SLOT_BYTES;  // FP8: converted tiles
     unsigned char *my_q = qslots + warp * kS * C::Q_BYTES;
     Cursor pc = locate(w0, s_pre, B);  // producer cursor
     Cursor cc = pc;                        // consumer cursor
@@ -318,14 +285,9 @@ __global__ void __launch_bounds__(kW * 32)
                 unsigned char *kdst = my_pipe + slot * C::SLOT_BYTES;
                 unsigned char *vdst = kdst + C::KV_BYTES;
                 const int row = (id * Hk + pc.j) * bs + (tok0 % bs);
-                if constexpr (F8) {
-                    // K: one swizzled box, read in place by the tile math; V: the
-                    // tile's rows are contiguous, one bulk copy
+                if constexpr (F8) {  // one swizzled box each, widened by the tile math
                     tma_load_2d(kdst, &tmap_k, 0, row, bar);
-                    bulk_copy_g2s(vdst,
-                                  static_cast<const unsigned char *>(a.v_cache) +
-                                      static_cast<size_t>(row) * D,
-                                  C::KV_BYTES, bar);
+                    tma_load_2d(vdst, &tmap_v, 0, row, bar);
                 } else {
 #pragma unroll
                     for (int bx = 0; bx < C::BOXES; ++bx) {
@@ -361,7 +323,7 @@ __global__ void __launch_bounds__(kW * 32)
     auto write_out = [&](int b, int j, float fm, float fl) {
         if (g >= G) return;
         const size_t bh = static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + g;
-        if (s_skip[b] > 0) {  // fold in the shared-prefix partial states
+        if (!F8 && s_skip[b] > 0) {  // fold in the shared-prefix partial states
             grid_dependency_wait();  // complete and visible once the shared pass is done
             const size_t r0 = bh * a.sh_parts;
             float M = fm;
@@ -394,10 +356,21 @@ __global__ void __launch_bounds__(kW * 32)
             fm = M;
         }
         const float inv = fl > 0.f ? a.v_scale / fl : 0.f;  // v_scale = 1 for fp16 caches
-        __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
+        if constexpr (F8) {  // columns 32c + 8tq .. + 7 (the E4M3 tile math's order)
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(a.out) + bh * D);
 #pragma unroll
-        for (int nb = 0; nb < C::NB_D; ++nb)
-            dst[nb * 4 + tq] = __floats2half2_rn(o[nb][0] * inv, o[nb][1] * inv);
+            for (int c = 0; c < D / 32; ++c)
+                dst[4 * c + tq] = make_uint4(
+                    pack_half2(o[4 * c][0] * inv, o[4 * c + 1][0] * inv),
+                    pack_half2(o[4 * c + 2][0] * inv, o[4 * c + 3][0] * inv),
+                    pack_half2(o[4 * c][1] * inv, o[4 * c + 1][1] * inv),
+                    pack_half2(o[4 * c + 2][1] * inv, o[4 * c + 3][1] * inv));
+        } else {
+            __half2 *dst = reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + bh * D);
+#pragma unroll
+            for (int nb = 0; nb < C::NB_D; ++nb)
+                dst[nb * 4 + tq] = __floats2half2_rn(o[nb][0] * inv, o[nb][1] * inv);
+        }
         if (tq == 0 && a.lse_out) a.lse_out[bh] = fl > 0.f ? (fm + log2f(fl)) * kLn2b : -INFINITY;
     };
 
@@ -526,11 +499,6 @@ __global__ void __launch_bounds__(kW * 32)
         last_t = cc.t;
         unsigned char *ks = my_pipe + slot * C::SLOT_BYTES;
         unsigned char *vs = ks + C::KV_BYTES;
-        if constexpr (F8) {  // widen the E4M3 V tile into the fp16 layout
-            e4m3_tile_to_f16<D>(vs, my_stage, lane);
-            __syncwarp();
-            vs = my_stage;
-        }
         const int n_valid =
             s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - (cc.t + s_skip[cc.b]) * kMmaTile) : 0;
         mma_tile<D, F8>(ks, vs, n_valid, qa, a.scale_log2, o, m_run, l_run, lane);
@@ -669,8 +637,9 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
 cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
                                    cudaStream_t stream) {
     const long long rows = a.num_blocks * a.n_kv_heads * static_cast<long long>(a.block_size);
-    CUtensorMap tk{}, tv{};  // E4M3 V tiles move by plain bulk copies, no tensor map
-    if (a.kv_fp8 ? !make_cache_map_e4m3(&tk, a.k_cache, rows, a.head_dim)
+    CUtensorMap tk{}, tv{};
+    if (a.kv_fp8 ? (!make_cache_map_e4m3(&tk, a.k_cache, rows, a.head_dim) ||
+                    !make_cache_map_e4m3(&tv, a.v_cache, rows, a.head_dim))
                  : (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
                     !make_cache_map(&tv, a.v_cache, rows, a.head_dim)))
         return cudaErrorNotSupported;

@@ -38,6 +38,13 @@ struct MmaCfg {
 // Byte offset of 16-byte unit `unit` (0-7) of row `row` in a 128B-swizzled box.
 __device__ __forceinline__ int swz(int row, int unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
 
+// The fp16 pair of E4M3 codes in bytes 0 (low half) and 1 of `two`.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
 // Piece p (as above) of row t of an E4M3 K tile staged by TMA with the D-byte
 // swizzle (D = 128: 128B, 16-byte unit u of row t at u ^ (t & 7); D = 64:
 // 64B, at u ^ ((t >> 1) & 3)), widened to the four fp16 pairs that the same
@@ -47,12 +54,16 @@ __device__ __forceinline__ uint4 e4m3_piece(const unsigned char *ks, int t, int 
     const int u = 4 * (p >> 1) + tq;  // 16-byte unit of the piece; it starts 8 * (p & 1) in
     const int off = D == 128 ? swz(t, u) : t * 64 + ((u ^ ((t >> 1) & 3)) << 4);
     const uint2 w = *reinterpret_cast<const uint2 *>(ks + off + 8 * (p & 1));
-    auto cvt2 = [](uint32_t two) {  // the low two codes of `two`
-        const __half2_raw h =
-            __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
-        return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-    };
-    return make_uint4(cvt2(w.x), cvt2(w.x >> 16), cvt2(w.y), cvt2(w.y >> 16));
+    return make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
+                      e4m3x2_to_f16x2(w.y >> 16));
+}
+
+// Byte offset of bytes [4c, 4c + 4) of row t of an E4M3 tile with the
+// D-byte swizzle (see e4m3_piece); c < D / 4.
+template <int D>
+__device__ __forceinline__ int e4m3_word_off(int t, int c) {
+    const int u = c >> 2;  // 16-byte unit
+    return (D == 128 ? swz(t, u) : t * 64 + ((u ^ ((t >> 1) & 3)) << 4)) + 4 * (c & 3);
 }
 
 // Q fragments of head g from a row-major [.., D] fp16 row (global or shared).
@@ -77,8 +88,15 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qa)[MmaCfg<D>::NP][4], co
 // One tile: rows [0, n_valid) of the K tile `ks` and V tile `vs` take part;
 // the V rows past n_valid are zeroed first (they may hold another sequence's
 // data or NaN and must not reach P.V).  Updates the running state of head g.
-// K8: `ks` is an E4M3 K tile (e4m3_piece), widened piece by piece.
-template <int D, bool K8 = false>
+//
+// F8: both tiles hold E4M3 codes with the D-byte swizzle, widened in
+// registers.  K goes piece by piece (e4m3_piece).  V needs, per lane, pairs
+// of tokens (2tq, 2tq+1) and (2tq+8, 2tq+9) of one column: the lane loads
+// 4-byte words of those four rows and pairs their bytes, so the output
+// columns are permuted instead of V being transposed.  Output block 4c + i,
+// column n, holds head_dim column 32c + 4n + i: o[4c + i][0] is column
+// 32c + 8tq + i and o[4c + i][1] is column 32c + 8tq + 4 + i (f8_out_col).
+template <int D, bool F8 = false>
 __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char *vs, int n_valid,
                                          const uint32_t (&qa)[MmaCfg<D>::NP][4],
                                          float scale_log2, float (&o)[MmaCfg<D>::NB_D][4],
@@ -87,12 +105,17 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
     const int g = lane >> 2;
     const int tq = lane & 3;
     if (n_valid < kMmaTile) {
-        const int per_row = C::BOXES * 8;
-        for (int idx = lane; idx < (kMmaTile - n_valid) * per_row; idx += 32) {
-            const int r = n_valid + idx / per_row;
-            const int rem = idx % per_row;
-            *reinterpret_cast<uint4 *>(vs + (rem >> 3) * C::BOX_BYTES + r * 128 + (rem & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (F8) {  // a row of codes is D contiguous bytes (swizzled within)
+            for (int idx = n_valid * (D / 16) + lane; idx < kMmaTile * (D / 16); idx += 32)
+                reinterpret_cast<uint4 *>(vs)[idx] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const int per_row = C::BOXES * 8;
+            for (int idx = lane; idx < (kMmaTile - n_valid) * per_row; idx += 32) {
+                const int r = n_valid + idx / per_row;
+                const int rem = idx % per_row;
+                *reinterpret_cast<uint4 *>(vs + (rem >> 3) * C::BOX_BYTES + r * 128 +
+                                           (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         fence_proxy_async_smem();  // before a later TMA write of these bytes
         __syncwarp();
@@ -107,7 +130,7 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
 #pragma unroll
         for (int p = 0; p < C::NP; ++p) {
             uint4 kw;
-            if constexpr (K8)
+            if constexpr (F8)
                 kw = e4m3_piece<D>(ks, t, p, tq);
             else
                 kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
@@ -151,17 +174,41 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
     }
     const uint32_t pa[4] = {pack_half2(pv[0][0], pv[0][1]), 0u, pack_half2(pv[1][0], pv[1][1]),
                             0u};
-    // O += P V: V fragments by transposed 8x8 loads, two 8-column blocks per load
-    const int lm = lane >> 3;
-    const int ri = lane & 7;
-    const int vt = ((lm & 1) << 3) + ri;
+    if constexpr (F8) {
+        // O += P V, E4M3 V: words of rows 2tq, 2tq+1, 2tq+8, 2tq+9 at column
+        // 32c + 4g; byte i of each row pair is output block 4c + i, column g
 #pragma unroll
-    for (int qd = 0; qd < C::NB_D / 2; ++qd) {
-        const int u = 2 * qd + (lm >> 1);
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
-        mma_16816(o[2 * qd], pa, r0, r1);
-        mma_16816(o[2 * qd + 1], pa, r2, r3);
+        for (int c = 0; c < D / 32; ++c) {
+            const int wc = 8 * c + g;  // 4-byte word of the row
+            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq, wc));
+            const uint32_t w1 =
+                *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 1, wc));
+            const uint32_t w2 =
+                *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 8, wc));
+            const uint32_t w3 =
+                *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 9, wc));
+            const uint32_t lo01 = __byte_perm(w0, w1, 0x5140);  // byte 0 pair, byte 1 pair
+            const uint32_t lo23 = __byte_perm(w0, w1, 0x7362);  // byte 2 pair, byte 3 pair
+            const uint32_t hi01 = __byte_perm(w2, w3, 0x5140);
+            const uint32_t hi23 = __byte_perm(w2, w3, 0x7362);
+            mma_16816(o[4 * c + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(hi01));
+            mma_16816(o[4 * c + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
+            mma_16816(o[4 * c + 2], pa, e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(hi23));
+            mma_16816(o[4 * c + 3], pa, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+        }
+    } else {
+        // O += P V: V fragments by transposed 8x8 loads, two 8-column blocks per load
+        const int lm = lane >> 3;
+        const int ri = lane & 7;
+        const int vt = ((lm & 1) << 3) + ri;
+#pragma unroll
+        for (int qd = 0; qd < C::NB_D / 2; ++qd) {
+            const int u = 2 * qd + (lm >> 1);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
+            mma_16816(o[2 * qd], pa, r0, r1);
+            mma_16816(o[2 * qd + 1], pa, r2, r3);
+        }
     }
 }
 
