@@ -342,7 +342,8 @@ def run_ours(args):
         P, ws_bytes = 0, pkv.decode_plan_fp8(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl)
     if multi:
         qstart = t(np.arange(B + 1, dtype=np.int32) * nq)
-        P, ws_bytes = pkv.multi_plan(B, B * nq, nq, H, Hk, D, bs, batch.max_blocks_per_seq, mcl)
+        P, ws_bytes = pkv.multi_plan(B, B * nq, nq, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
+                                     args.partition)
     # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
     launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 and P > 0 else 0)
     groups = None

@@ -557,15 +557,20 @@ int make_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads, int
     mp->row_blocks = pkv::multi_row_blocks(max_q_len > 0 ? max_q_len : 1, group);
     int P = partition_tokens;
     if (P == 0) {
-        // the largest power of two in [64, 2048] whose grid still has about
-        // eight CTAs per SM (a CTA serves up to four row blocks)
+        // the largest power of two in [64, 1024] whose grid still has about
+        // eight CTAs per SM (a CTA serves up to four row blocks), and at most
+        // a quarter of the longest context: with skewed lengths one long
+        // sequence's partitions otherwise set the time (Mistral-shaped mix,
+        // two tokens per sequence: 146 us at 2048, 96 at 1024, 82 at 256;
+        // 2048 was never the fastest in a sweep over the five workloads)
         int sms = 0;
         const int rc = sm_count(&sms);
         if (rc != PKV_OK) return rc;
-        P = 2048;
+        P = 1024;
         const int groups = (mp->row_blocks + 3) / 4;
         const long long items = static_cast<long long>(num_seqs) * n_kv_heads * groups;
         while (P > 64 && items * ((max_len + P - 1) / P) < 8LL * sms) P /= 2;
+        while (P > 64 && 4LL * P > max_len) P /= 2;
     } else if (P < 16 || P % 16 != 0 || P % block_size != 0) {
         return PKV_ERR_INVALID_ARG;
     }
