@@ -3,7 +3,7 @@
 //
 // The work of one call is the list of (KV head j, sequence b, 16-token tile t)
 // units, ordered j, then b, then t: T units in all.  The W warps of the grid
-// (W = 4 x number of CTAs, sized to fill every SM once) take consecutive
+// (4 or 8 per CTA, the grid sized to fill every SM once) take consecutive
 // ranges of U = max(4, ceil(T / W)) units each, so every working warp moves the
 // same number of K/V bytes whatever the mix of context lengths.  A warp streams its range
 // through its own ring of TMA-loaded tiles, carrying the online-softmax state
@@ -22,7 +22,6 @@
 // partial results from FlashAttention-2 (section 14 references).
 #include <cuda.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
