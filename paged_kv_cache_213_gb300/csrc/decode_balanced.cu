@@ -52,6 +52,12 @@ constexpr int kMinUnits = 4;        // fewest units a working warp takes
 // (forked completions: a block or two), and each output waits for the shared
 // pass; one short segment per warp spreads those fold-ins over more warps.
 constexpr int kMinUnitsSuffix = 2;
+// With eight warps per CTA (long segments, most of them cut), the split
+// counts every segment start as this many extra units.  A warp whose range
+// holds a segment's first tile is the one that releases the cut piece before
+// it, mid-loop (a GPU-scope release while its loads are in flight, about two
+// tiles' time), so it gets about that much less to stream.
+constexpr int kCutUnits = 2;
 constexpr float kLn2b = 0.69314718055994531f;
 
 template <int D, int G, bool F8, int kW>
@@ -133,12 +139,14 @@ __global__ void __launch_bounds__(kW * 32)
     __shared__ uint64_t merge_bar[kW];
     __shared__ int s_ok[kW][kS];
     __shared__ int s_scan[kW];
+    __shared__ int s_scan_nz[kW];
     const uint32_t raw_s = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
     unsigned char *qslots = smem + C::PIPE_BYTES;
     int *s_pre = reinterpret_cast<int *>(qslots + C::QS_BYTES);  // [B + 1]
     int *s_len = s_pre + a.num_seqs + 1;                          // [B]
     int *s_skip = s_len + a.num_seqs;  // [B] tiles left to the shared-prefix pass
+    int *s_nz = s_skip + a.num_seqs;   // [B + 1] sequences with tiles before b
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -187,24 +195,46 @@ __global__ void __launch_bounds__(kW * 32)
         }
         __syncthreads();
     }
-    int local = 0;
-    for (int b = c0; b < c1; ++b) local += (s_len[b] + kMmaTile - 1) / kMmaTile - s_skip[b];
-    int incl = local;
+    // tiles per sequence and sequences with tiles, both prefix-summed
+    auto tiles_of = [&](int b) { return (s_len[b] + kMmaTile - 1) / kMmaTile - s_skip[b]; };
+    int local = 0, local_nz = 0;
+    for (int b = c0; b < c1; ++b) {
+        const int tb = tiles_of(b);
+        local += tb;
+        local_nz += tb > 0;
+    }
+    int incl = local, incl_nz = local_nz;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
+        const int v_nz = __shfl_up_sync(0xffffffffu, incl_nz, off);
+        if (lane >= off) {
+            incl += v;
+            incl_nz += v_nz;
+        }
     }
-    if (lane == 31) s_scan[warp] = incl;
+    if (lane == 31) {
+        s_scan[warp] = incl;
+        s_scan_nz[warp] = incl_nz;
+    }
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += s_scan[w];
-    int run = base + incl - local;
+    int base = 0, base_nz = 0;
+    for (int w = 0; w < warp; ++w) {
+        base += s_scan[w];
+        base_nz += s_scan_nz[w];
+    }
+    int run = base + incl - local, run_nz = base_nz + incl_nz - local_nz;
     for (int b = c0; b < c1; ++b) {
         s_pre[b] = run;
-        run += (s_len[b] + kMmaTile - 1) / kMmaTile - s_skip[b];
+        s_nz[b] = run_nz;
+        const int tb = tiles_of(b);
+        run += tb;
+        run_nz += tb > 0;
     }
-    if (tid == kThreadsB - 1) s_pre[B] = base + incl;
+    if (tid == kThreadsB - 1) {
+        s_pre[B] = base + incl;
+        s_nz[B] = base_nz + incl_nz;
+    }
     __syncthreads();
 
     // Sequences without private tiles (sequences spread over the CTAs): empty
@@ -233,13 +263,41 @@ __global__ void __launch_bounds__(kW * 32)
         }
     }
 
-    // --- this warp's range of units: [w * U, (w + 1) * U) clipped to T
+    // --- this warp's range of units.  The split is even over "virtual"
+    // units: each segment (b, j) with tiles is kCut units, then its tiles.
+    // Unit x of segment number s (in j, b order) sits at virtual position
+    // x + kCut * (s + 1); warp w takes the units whose positions fall in
+    // [w * U, (w + 1) * U).  kCut = 0: the plain even split.
+    constexpr int kCut = kW == kWLarge ? kCutUnits : 0;
     const int w = blockIdx.x * kW + warp;
-    const int T = Hk * s_pre[B];
+    const int TB = s_pre[B];
+    const int T = Hk * TB;
+    const int NZ = s_nz[B];
+    const long long VTB = TB + static_cast<long long>(kCut) * NZ;
+    const long long VT = Hk * VTB;
     // at least kMinUnits units per warp: short segments then stay whole
-    const int U = max(a.num_groups > 0 ? kMinUnitsSuffix : kMinUnits, (T + workers - 1) / workers);
-    const int w0 = static_cast<int>(min(static_cast<long long>(T), static_cast<long long>(w) * U));
-    const int n = min(T, w0 + U) - w0;
+    const int U = static_cast<int>(max(static_cast<long long>(a.num_groups > 0 ? kMinUnitsSuffix
+                                                                               : kMinUnits),
+                                       (VT + workers - 1) / workers));
+    auto real_at = [&](long long v) -> int {  // the first unit at or after position v
+        if (v >= VT) return T;
+        const int j = static_cast<int>(v / VTB);
+        const int r = static_cast<int>(v - j * VTB);
+        int lo = 0, hi = B - 1;  // the last sequence whose segment starts at or before r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_pre[mid] + kCut * s_nz[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        const int off = r - (s_pre[lo] + kCut * s_nz[lo]);
+        const int x0 = j * TB + s_pre[lo];
+        return off < kCut ? x0 : x0 + off - kCut;
+    };
+    // virtual position of the first unit of segment (b, j), and of the unit before it
+    auto vpos0 = [&](int b, int j) {
+        return j * TB + s_pre[b] + kCut * (j * NZ + s_nz[b] + 1);
+    };
+    const int w0 = real_at(static_cast<long long>(w) * U);
+    const int n = real_at(static_cast<long long>(w + 1) * U) - w0;
     if (n <= 0) return;  // no CTA-wide barriers below
 
     unsigned char *my_pipe = smem + warp * C::WARP_BYTES;
@@ -400,8 +458,8 @@ __global__ void __launch_bounds__(kW * 32)
         }
         __syncwarp();  // the record's stores, all lanes, before lane 0's release
         const int x0 = pj * s_pre[B] + s_pre[pb];  // the segment's units [x0, x0 + nt)
-        const int wf = x0 / U;
-        const int wl = (x0 + nt - 1) / U;
+        const int wf = vpos0(pb, pj) / U;          // the warps holding its pieces
+        const int wl = (vpos0(pb, pj) + nt - 1) / U;
         // lane 1 counts: lane 0 issues the ring's TMA loads, and a release by
         // the lane that issued them could wait for them to land
         int old = 0;
@@ -425,9 +483,12 @@ __global__ void __launch_bounds__(kW * 32)
         // the acquiring atomic (lane 0) made the other warps' records visible;
         // order them before the bulk copies (async proxy) that read them
         asm volatile("fence.proxy.async.global;" ::: "memory");
-        const int wf = x0 / U;
-        const int wl = (x0 + nt - 1) / U;
-        const bool wf_starts_here = wf * U == x0;
+        const int v0 = vpos0(b, j);
+        const int wf = v0 / U;
+        const int wl = (v0 + nt - 1) / U;
+        // the piece in warp wf is its first iff the unit before x0 (at
+        // position v0 - kCut - 1) lies before warp wf's positions
+        const bool wf_starts_here = x0 == 0 || static_cast<long long>(wf) * U > v0 - kCut - 1;
         constexpr int cap = static_cast<int>(C::WARP_BYTES / REC);
         float M = -INFINITY, Lsum = 0.f;
 #pragma unroll
@@ -529,7 +590,7 @@ __global__ void __launch_bounds__(kW * 32)
 template <int D, int G, bool F8, int kW>
 size_t bal_smem(int B) {
     using C = BalCfg<D, G, F8, kW>;
-    return 1024 + C::PIPE_BYTES + C::QS_BYTES + (3 * static_cast<size_t>(B) + 1) * 4;
+    return 1024 + C::PIPE_BYTES + C::QS_BYTES + (4 * static_cast<size_t>(B) + 2) * 4;
 }
 
 template <int D, int G, bool F8, int kW>
@@ -617,10 +678,12 @@ bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
 #undef PKV_BAL_OCC
     if (per_sm <= 0) return false;
     if (few && per_sm * warps > kWLarge) per_sm = kWLarge / warps > 0 ? kWLarge / warps : 1;
-    // units must fit 32-bit arithmetic: Hk * B * tiles per sequence
+    // units must fit 32-bit arithmetic: Hk * B * (tiles per sequence + the
+    // split's extra units per segment)
     const long long t_max = static_cast<long long>(n_kv_heads) * num_seqs *
                             ((static_cast<long long>(max_len) + kMmaTile - 1) / kMmaTile);
-    if (t_max >= (1LL << 31)) return false;
+    if (t_max + static_cast<long long>(kCutUnits) * n_kv_heads * num_seqs >= (1LL << 31))
+        return false;
     long long ctas = static_cast<long long>(sms) * per_sm;
     const long long need = (t_max + 2 * warps - 1) / (2 * warps);  // >= 2 tiles per warp on average
     if (need < ctas) ctas = need;
