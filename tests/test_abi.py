@@ -132,3 +132,94 @@ def test_fp8_host_rejections(lib):
     att.restype = c.c_int
     assert att(x, x, x, x, x, x, 4, 8, 10, 0.1, -1.0, 1.0, 8, 2, 128, 16, 0, x, 1 << 20, None,
                None, None) == -1
+
+
+def _multi_fns(lib):
+    c = ctypes
+    p = c.c_void_p
+    plan = lib.paged_decode_multi_plan
+    plan.argtypes = [c.c_int] * 10 + [c.POINTER(c.c_int), c.POINTER(c.c_size_t)]
+    plan.restype = c.c_int
+    att = lib.paged_decode_attention_multi
+    att.argtypes = [p, p, p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64,
+                    c.c_float, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p,
+                    c.c_size_t, p, p, p]
+    att.restype = c.c_int
+    return plan, att
+
+
+def _multi_plan(plan, *args):
+    P = ctypes.c_int(-1)
+    W = ctypes.c_size_t(0)
+    rc = plan(*args, ctypes.byref(P), ctypes.byref(W))
+    return rc, P.value, W.value
+
+
+def test_multi_plan_explicit_partition(lib):
+    plan, _ = _multi_fns(lib)
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # B=4, 8 query rows, <= 2 per sequence, 8/2 heads, d=128, bs=16, 16 blocks per
+    # table, longest context 256, 64-token partitions: 4 partitions per row
+    rc, P, W = _multi_plan(plan, 4, 8, 2, 8, 2, 128, 16, 16, 256, 64)
+    rows = 8 * 8 * 4
+    assert rc == 0 and P == 64 and W == up(rows * 128 * 4) + 2 * up(rows * 4)
+    # one partition covers the longest context: no workspace
+    rc, P, W = _multi_plan(plan, 4, 8, 2, 8, 2, 128, 16, 16, 64, 64)
+    assert rc == 0 and W == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((4, 8, 2, 6, 4, 128, 16, 16, 256, 64), -1),    # 6 % 4 != 0
+    ((4, 8, 2, 8, 2, 96, 16, 16, 256, 64), -2),     # head_dim 96 not built
+    ((4, 8, 2, 8, 2, 128, 8, 16, 256, 64), -2),     # block size not a multiple of 16
+    ((4, 8, 2, 6, 2, 128, 16, 16, 256, 64), -2),    # group 3
+    ((4, 8, 2, 8, 2, 128, 16, 16, 256, 24), -1),    # partition not a multiple of 16
+    ((-1, 8, 2, 8, 2, 128, 16, 16, 256, 64), -1),
+    ((4, 8, 2, 8, 2, 128, 16, 0, 256, 64), -1),     # no blocks per table
+])
+def test_multi_plan_rejects(lib, args, status):
+    plan, _ = _multi_fns(lib)
+    assert _multi_plan(plan, *args)[0] == status
+
+
+def test_multi_call_rejects_bad_arguments_without_launching(lib):
+    _, att = _multi_fns(lib)
+    n = None
+    x = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    ws = ctypes.c_void_p(1 << 24)
+
+    def call(out=x, q=x, qs=x, num_blocks=40, scale=0.1, B=4, ws_ptr=ws, ws_bytes=1 << 22,
+             max_len=256, P=64):
+        return att(out, q, x, x, x, x, qs, B, 8, 2, 16, num_blocks, scale, 8, 2, 128, 16,
+                   max_len, P, ws_ptr, ws_bytes, n, n, n)
+    assert call(num_blocks=0) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(out=n) == -1
+    assert call(q=odd) == -1
+    assert call(qs=n) == -1
+    assert call(ws_ptr=n) == -3                       # 4 partitions, no workspace
+    assert call(ws_bytes=64) == -3
+    assert call(B=0) == 0                             # nothing to do
+    assert call(num_blocks=1 << 27) == -2             # TMA rows past 32 bits
+
+
+def test_prefix_shared_call_rejects_bad_arguments(lib):
+    c = ctypes
+    p = c.c_void_p
+    fn = lib.paged_decode_attention_prefix_shared
+    fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float, c.c_int, c.c_int,
+                   c.c_int, c.c_int, c.c_int, p, p, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p,
+                   p, p]
+    fn.restype = c.c_int
+    x = p(1 << 20)
+    odd = p((1 << 20) + 2)
+
+    def call(num_blocks=40, scale=0.1, offs=x, pref=x, groups=2):
+        return fn(x, x, x, x, x, x, 4, 8, num_blocks, scale, 8, 2, 128, 16, 256, offs, pref,
+                  groups, 2, 64, x, 1 << 22, None, None, None)
+    assert call(num_blocks=0) == -1
+    assert call(scale=float("inf")) == -1
+    assert call(offs=None) == -1                      # groups without their offsets
+    assert call(pref=None) == -1
+    assert call(offs=odd) == -1                       # int32 arrays must be 4-byte aligned
