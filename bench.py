@@ -8,9 +8,12 @@ from N(0, 1)).
 Prints one JSON line.  `value` is the step's algorithmic bytes (unique K/V
 rows read + Q + O + block tables + context lengths + the append's reads and
 writes) divided by the mean device time of one step, in GB/s.  Steps run as
-CUDA-graph replays with timing events inside the graph; L2 is flushed
-before every step (a 2x-L2 buffer is written, then a second one is read so
-that L2 holds clean lines), outside the timed events.
+CUDA-graph replays with timing events inside the graph, back to back: the
+steps cycle through four device copies of the workload's inputs, each larger
+than L2, so that no step finds its inputs in L2.  The same calls are also
+timed one at a time, each after an L2 flush (a 2x-L2 buffer is written, then
+a second one is read so that L2 holds clean lines) and between its own two
+events, so that each pays its own launch latency (the `_isolated` keys).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -65,6 +68,8 @@ def parse_args(argv=None):
                     help="query tokens per sequence: > 1 times the multi-token causal call "
                          "(speculative verify) instead of the decode step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the attention-only rows of workloads 3, 4 and 5")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
 
@@ -239,19 +244,26 @@ def oracle_threads():
         return os.cpu_count() or 1
 
 
-def oracle_step_sample(batch, seqs, threads):
+def oracle_step_sample(batch, seqs, threads, work=None):
     """Run the oracle's append + decode for the sequences `seqs` (all heads);
-    returns (seconds, bytes of that sample)."""
+    returns (seconds, bytes of that sample).
+
+    work: (k_cache, v_cache) working copies, made once outside the timed
+    region; the append writes only the sampled sequences' slots into them, in
+    place (rewriting a slot with the same token leaves the copies valid for
+    the next sample)."""
     import oracle
     B, H = batch.num_seqs, batch.n_q_heads
     mask = np.zeros((B, H), dtype=bool)
     mask[list(seqs)] = True
+    if work is None:
+        work = (batch.k_cache.copy(), batch.v_cache.copy())
+    kc, vc = work
     t0 = time.perf_counter()
-    kc, vc = batch.k_cache, batch.v_cache
     if batch.has_append:
-        keep = np.isin(np.arange(batch.slot_mapping.shape[0]), list(seqs))
-        slots = np.where(keep, batch.slot_mapping, -1)
-        kc, vc = oracle.append(batch.k_new, batch.v_new, slots, kc, vc, batch.block_size)
+        sel = [b for b in seqs if b < batch.slot_mapping.shape[0]]
+        oracle.append_inplace(batch.k_new[sel], batch.v_new[sel], batch.slot_mapping[sel], kc, vc,
+                              batch.block_size)
     oracle.decode(batch.q, kc, vc, batch.block_tables, batch.context_lens, batch.scale,
                   batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size,
                   mask=mask, num_threads=threads)
@@ -268,8 +280,9 @@ def cpu_baseline(batch, seconds):
     threads = oracle_threads()
     total_t, total_b, steps = 0.0, 0, 0
     everything = range(batch.num_seqs)
+    work = (batch.k_cache.copy(), batch.v_cache.copy())
     while total_t < seconds or steps == 0:
-        dt, nb = oracle_step_sample(batch, everything, threads)
+        dt, nb = oracle_step_sample(batch, everything, threads, work)
         total_t += dt
         total_b += nb
         steps += 1
@@ -282,6 +295,281 @@ def cpu_baseline(batch, seconds):
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
+
+# Back-to-back timing cycles through this many device copies of a workload's
+# inputs: each copy is larger than L2, so a launch finds none of its inputs
+# left in L2 by the launch before it.
+ROTATE = 4
+
+
+class Path:
+    """Device inputs (ROTATE copies) and the library calls of one timed path:
+    `step(i)` = one decode step on copy i (append + attention, or attention
+    alone), `attend(i)` = the attention call alone."""
+
+    def __init__(self, pkv, wl, torch, batch, device, *, fp8=False, q_len=1, prefix=False,
+                 partition=0, copies=ROTATE, q_seed=20300):
+        self.batch = batch
+        self.fp8, self.nq = fp8, max(1, q_len)
+        self.multi = self.nq > 1
+        B, H, Hk, D, bs = batch.num_seqs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, \
+            batch.block_size
+        MB, mcl = batch.max_blocks_per_seq, batch.max_context_len
+        self.has_append = batch.has_append and not self.multi
+
+        def t(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+        if self.multi:
+            rng_q = np.random.default_rng(q_seed)
+            qh = rng_q.standard_normal((B * self.nq, H, D)).astype(np.float16)
+        else:
+            qh = batch.q
+        first = {"q": t(qh), "kc": t(batch.k_cache), "vc": t(batch.v_cache),
+                 "bt": t(batch.block_tables), "cl": t(batch.context_lens)}
+        self.k_scale = self.v_scale = 1.0
+        if fp8:
+            # per-tensor scales max|x| / 448; the caches' E4M3 codes made by torch
+            # (input preparation, outside the timed path)
+            def amax(*xs):
+                return max(float(np.max(np.abs(x.astype(np.float32)))) for x in xs)
+            extra_k = [batch.k_new] if self.has_append else []
+            extra_v = [batch.v_new] if self.has_append else []
+            self.k_scale = np.float32(amax(batch.k_cache, *extra_k) / 448)
+            self.v_scale = np.float32(amax(batch.v_cache, *extra_v) / 448)
+            for key, sc in (("kc", self.k_scale), ("vc", self.v_scale)):
+                first[key] = (first[key].float() / float(sc)).clamp(-448, 448) \
+                    .to(torch.float8_e4m3fn).view(torch.uint8)
+        if self.has_append:
+            first.update(kn=t(batch.k_new), vn=t(batch.v_new), sm=t(batch.slot_mapping))
+        if self.multi:
+            first["qstart"] = t(np.arange(B + 1, dtype=np.int32) * self.nq)
+        self.P, self.ws_bytes = pkv.decode_plan(B, H, Hk, D, bs, MB, mcl, partition)
+        if fp8:
+            self.P, self.ws_bytes = 0, pkv.decode_plan_fp8(B, H, Hk, D, bs, MB, mcl)
+        if self.multi:
+            self.P, self.ws_bytes = pkv.multi_plan(B, B * self.nq, self.nq, H, Hk, D, bs, MB,
+                                                   mcl, partition)
+        # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
+        self.attn_launches = 1 + (1 if self.ws_bytes > 0 and self.P > 0 else 0)
+        self.groups = None
+        if prefix and batch.meta.get("shared") and not fp8 and not self.multi:
+            offs, pref, gmax, pmax = wl.prefix_groups(batch)
+            first["offs"], first["pref"] = t(offs), t(pref)
+            self.groups = (gmax, pmax, len(pref))
+            self.ws_bytes = pkv.prefix_shared_plan(B, H, Hk, D, bs, MB, mcl, len(pref), gmax,
+                                                   pmax)
+            self.attn_launches = 2
+        self.step_launches = self.attn_launches + (1 if self.has_append else 0)
+        self.copies = [first] + [{k: v.clone() for k, v in first.items()}
+                                 for _ in range(copies - 1)]
+        for c in self.copies:
+            c["out"] = torch.empty_like(c["q"])
+            c["work"] = torch.zeros(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+            c["err"] = torch.zeros(1, dtype=torch.int32, device=device)
+        self.pkv = pkv
+
+    def attend(self, i):
+        pkv, bt, c = self.pkv, self.batch, self.copies[i]
+        H, Hk, D, bs, mcl = bt.n_q_heads, bt.n_kv_heads, bt.head_dim, bt.block_size, \
+            bt.max_context_len
+        ws = c["work"] if self.ws_bytes > 0 else None
+        if self.multi:
+            pkv.paged_decode_attention_multi(c["q"], c["kc"], c["vc"], c["bt"], c["cl"],
+                                             c["qstart"], bt.scale, H, Hk, D, bs, self.nq,
+                                             max_context_len=mcl, partition_tokens=self.P,
+                                             out=c["out"], workspace=ws, err_word=c["err"])
+        elif self.fp8:
+            pkv.paged_decode_attention_fp8(c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale,
+                                           self.k_scale, self.v_scale, H, Hk, D, bs,
+                                           max_context_len=mcl, out=c["out"], workspace=ws,
+                                           err_word=c["err"])
+        elif self.groups is not None:
+            gmax, pmax, _ = self.groups
+            pkv.paged_decode_attention_prefix_shared(
+                c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale, H, Hk, D, bs, c["offs"],
+                c["pref"], gmax, pmax, max_context_len=mcl, out=c["out"], workspace=ws,
+                err_word=c["err"])
+        else:
+            pkv.paged_decode_attention(c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale, H,
+                                       Hk, D, bs, max_context_len=mcl, partition_tokens=self.P,
+                                       out=c["out"], workspace=ws, err_word=c["err"])
+
+    def step(self, i):
+        """append + attention: one library call when the step has an append on
+        the default (fp16, one query token) path, so that the attention's
+        prologue overlaps the append."""
+        pkv, bt, c = self.pkv, self.batch, self.copies[i]
+        if not self.has_append:
+            self.attend(i)
+            return
+        if self.fp8:
+            pkv.paged_kv_append_fp8(c["kn"], c["vn"], c["sm"], c["kc"], c["vc"], self.k_scale,
+                                    self.v_scale, err_word=c["err"])
+            self.attend(i)
+            return
+        if self.groups is not None:
+            pkv.paged_kv_append(c["kn"], c["vn"], c["sm"], c["kc"], c["vc"], err_word=c["err"])
+            self.attend(i)
+            return
+        pkv.paged_decode_step(c["kn"], c["vn"], c["sm"], c["q"], c["kc"], c["vc"], c["bt"],
+                              c["cl"], bt.scale, bt.n_q_heads, bt.n_kv_heads, bt.head_dim,
+                              bt.block_size, max_context_len=bt.max_context_len,
+                              partition_tokens=self.P, out=c["out"],
+                              workspace=c["work"] if self.ws_bytes > 0 else None,
+                              err_word=c["err"])
+
+    def errors(self):
+        return [self.pkv.get_error(c["err"]) for c in self.copies]
+
+
+class Timer:
+    """CUDA-event timing inside CUDA-graph replays (eager launches when this
+    torch cannot record events inside a graph).
+
+    isolated(): every call is its own timed region -- flush L2, event, call,
+      event -- so each call starts cold and pays its own launch latency.
+    back_to_back(): S calls in a row between two events, cycling through the
+      input copies (each larger than L2, so no call finds its inputs in L2);
+      a call's launch overlaps the call before it, as in a serving step where
+      the attention follows other kernels.  One figure per graph replay: the
+      interval divided by S.
+    """
+
+    def __init__(self, torch, device, graph_steps):
+        self.torch, self.device, self.S = torch, device, max(1, graph_steps)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.flush_w = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+        self.flush_r = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+        self.sink = torch.empty(1, dtype=torch.float32, device=device)
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+            self.in_graph = True
+        except TypeError:
+            self.in_graph = False
+        self.side = torch.cuda.Stream(device)
+
+    def flush(self):
+        """L2 flush: write a 2xL2 buffer, then read another 2xL2 buffer so
+        that L2 holds only clean lines."""
+        self.flush_w.zero_()
+        self.torch.sum(self.flush_r, dim=0, out=self.sink[0])
+
+    def _ev(self):
+        return self.torch.cuda.Event(enable_timing=True, external=self.in_graph)
+
+    def _graph(self, record):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        self.side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.graph(g, stream=self.side):
+            record()
+        torch.cuda.synchronize()
+        g.replay()  # one untimed replay after capture
+        torch.cuda.synchronize()
+        return g
+
+    def isolated(self, body, steps, eager=False):
+        """Per-call device times (ms) of `body(i)` (i = the call's index)."""
+        torch, S = self.torch, min(self.S, steps)
+        out = []
+        if self.in_graph and not eager:
+            evs = [(self._ev(), self._ev()) for _ in range(S)]
+
+            def record():
+                for i in range(S):
+                    self.flush()
+                    evs[i][0].record()
+                    body(i)
+                    evs[i][1].record()
+            g = self._graph(record)
+            while len(out) < steps:
+                g.replay()
+                torch.cuda.synchronize()
+                out += [a.elapsed_time(b) for a, b in evs][:steps - len(out)]
+            return out
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            self.flush()
+            evs[i][0].record()
+            body(i)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def back_to_back(self, body, steps):
+        """Per-call device times (ms), one per replay of S back-to-back calls
+        of `body(i)`, S the largest divisor of `steps` up to the graph size:
+        exactly `steps` calls are timed."""
+        torch = self.torch
+        S = max(d for d in range(1, min(self.S, steps) + 1) if steps % d == 0)
+        self.last_s = S
+        out = []
+        if self.in_graph:
+            e0, e1 = self._ev(), self._ev()
+
+            def record():
+                self.flush()
+                e0.record()
+                for i in range(S):
+                    body(i)
+                e1.record()
+            g = self._graph(record)
+            for _ in range(max(1, -(-steps // S))):
+                g.replay()
+                torch.cuda.synchronize()
+                out.append(e0.elapsed_time(e1) / S)
+            return out
+        for _ in range(max(1, -(-steps // S))):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            self.flush()
+            e0.record()
+            for i in range(S):
+                body(i)
+            e1.record()
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) / S)
+        return out
+
+
+def per_config_rows(pkv, wl, torch, device, timer, peak, steps, workloads):
+    """Attention-only rows for the other standard workloads, timed like the
+    headline (both ways); the prefix-aware entry point too where the workload
+    shares prefix blocks."""
+    rows = {}
+    for w in workloads:
+        batch = wl.workload(w, poison=False)
+        if batch.has_append:  # attention over the cache as generated
+            batch.slot_mapping = batch.k_new = batch.v_new = None
+        nbytes = workload_bytes(batch)["attention"]
+        variants = [("regular", False)] + ([("prefix_shared", True)]
+                                           if batch.meta.get("shared") else [])
+        for name, prefix in variants:
+            path = Path(pkv, wl, torch, batch, device, prefix=prefix)
+            for i in range(3):
+                timer.flush()
+                path.attend(i % ROTATE)
+            torch.cuda.synchronize()
+            b2b = timer.back_to_back(lambda i: path.attend(i % ROTATE), steps)
+            iso = timer.isolated(lambda i: path.attend(i % ROTATE), min(steps, 200))
+            if any(path.errors()):
+                raise SystemExit(f"bench.py: device error word on workload {w} ({name})")
+            ms, ms_iso = statistics.fmean(b2b), statistics.fmean(iso)
+            rows[f"w{w}_{name}"] = {
+                "workload": wl.WORKLOADS[w], "entry": "paged_decode_attention_prefix_shared"
+                if prefix else "paged_decode_attention",
+                "attention_bytes": nbytes, "attention_ms": round(ms, 5),
+                "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
+                "attention_ms_isolated": round(ms_iso, 5),
+                "frac_isolated": round(nbytes / (ms_iso * 1e-3) / 1e9 / peak, 4),
+                "percentiles_ms": pcts(b2b), "percentiles_ms_isolated": pcts(iso),
+                "launches_per_call": path.attn_launches,
+            }
+            del path
+            torch.cuda.empty_cache()
+    return rows
+
 
 def run_ours(args):
     import torch
@@ -304,218 +592,54 @@ def run_ours(args):
         # n new tokens per sequence, already in the cache: an attention-only step
         # whose Q and O carry n rows per sequence
         batch.slot_mapping = batch.k_new = batch.v_new = None
-        rng_q = np.random.default_rng(20300 + args.workload)
-        q_multi = rng_q.standard_normal((batch.num_seqs * nq, batch.n_q_heads,
-                                         batch.head_dim)).astype(np.float16)
     nbytes = workload_bytes(batch, 1 if fp8 else 2)
     if multi:
         extra = 2 * (nq - 1) * batch.num_seqs * batch.n_q_heads * batch.head_dim * 2
         for key in ("step", "attention", "logical_step"):
             nbytes[key] += extra
-
-    def t(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
-
-    q, kc, vc = t(q_multi if multi else batch.q), t(batch.k_cache), t(batch.v_cache)
-    k_scale = v_scale = 1.0
-    if fp8:
-        # per-tensor scales max|x| / 448; the caches' E4M3 codes made by torch
-        # (input preparation, outside the timed path)
-        def amax(*xs):
-            return max(float(np.max(np.abs(x.astype(np.float32)))) for x in xs)
-        k_scale = np.float32(amax(batch.k_cache, *([batch.k_new] if batch.has_append else [])) / 448)
-        v_scale = np.float32(amax(batch.v_cache, *([batch.v_new] if batch.has_append else [])) / 448)
-        kc = (kc.float() / float(k_scale)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
-        vc = (vc.float() / float(v_scale)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
-    bt, cl = t(batch.block_tables), t(batch.context_lens)
-    has_append = batch.has_append
-    if has_append:
-        kn, vn, sm = t(batch.k_new), t(batch.v_new), t(batch.slot_mapping)
-    out = torch.empty_like(q)
-    err = torch.zeros(1, dtype=torch.int32, device=device)
+    path = Path(pkv, wl, torch, batch, device, fp8=fp8, q_len=nq, prefix=args.prefix_shared,
+                partition=args.partition, q_seed=20300 + args.workload)
+    has_append = path.has_append
     B, H, Hk, D, bs = batch.num_seqs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, \
         batch.block_size
-    mcl = batch.max_context_len
-    P, ws_bytes = pkv.decode_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
-                                  args.partition)
-    if fp8:
-        P, ws_bytes = 0, pkv.decode_plan_fp8(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl)
-    if multi:
-        qstart = t(np.arange(B + 1, dtype=np.int32) * nq)
-        P, ws_bytes = pkv.multi_plan(B, B * nq, nq, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
-                                     args.partition)
-    # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
-    launches_per_step = (1 if has_append else 0) + 1 + (1 if ws_bytes > 0 and P > 0 else 0)
-    groups = None
-    if args.prefix_shared and batch.meta.get("shared") and not fp8:
-        offs, pref, gmax, pmax = wl.prefix_groups(batch)
-        groups = (t(offs), t(pref), gmax, pmax)
-        ws_bytes = pkv.prefix_shared_plan(B, H, Hk, D, bs, batch.max_blocks_per_seq, mcl,
-                                          len(pref), gmax, pmax)
-        launches_per_step = (1 if has_append else 0) + 2
-    work = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    timer = Timer(torch, device, args.graph_steps)
 
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush_w = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
-    flush_r = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
-    sink = torch.empty(1, dtype=torch.float32, device=device)
-
-    def flush():
-        flush_w.zero_()
-        torch.sum(flush_r, dim=0, out=sink[0])
-
-    def append():
-        if has_append and fp8:
-            pkv.paged_kv_append_fp8(kn, vn, sm, kc, vc, k_scale, v_scale, err_word=err)
-        elif has_append:
-            pkv.paged_kv_append(kn, vn, sm, kc, vc, err_word=err)
-
-    def attend():
-        if multi:
-            pkv.paged_decode_attention_multi(q, kc, vc, bt, cl, qstart, batch.scale, H, Hk, D,
-                                             bs, nq, max_context_len=mcl, partition_tokens=P,
-                                             out=out, workspace=work if ws_bytes > 0 else None,
-                                             err_word=err)
-            return
-        if fp8:
-            pkv.paged_decode_attention_fp8(q, kc, vc, bt, cl, batch.scale, k_scale, v_scale, H,
-                                           Hk, D, bs, max_context_len=mcl, out=out,
-                                           workspace=work, err_word=err)
-            return
-        if groups is not None:
-            pkv.paged_decode_attention_prefix_shared(
-                q, kc, vc, bt, cl, batch.scale, H, Hk, D, bs, groups[0], groups[1], groups[2],
-                groups[3], max_context_len=mcl, out=out, workspace=work, err_word=err)
-            return
-        pkv.paged_decode_attention(q, kc, vc, bt, cl, batch.scale, H, Hk, D, bs,
-                                   max_context_len=mcl, partition_tokens=P, out=out,
-                                   workspace=work if ws_bytes > 0 else None, err_word=err)
-
-    def step():
-        """append + attention: one library call when the step has an append on
-        the default (fp16, one query token) path, so that the attention's
-        prologue overlaps the append."""
-        if has_append and not fp8 and not multi and groups is None:
-            pkv.paged_decode_step(kn, vn, sm, q, kc, vc, bt, cl, batch.scale, H, Hk, D, bs,
-                                  max_context_len=mcl, partition_tokens=P, out=out,
-                                  workspace=work if ws_bytes > 0 else None, err_word=err)
-        else:
-            append()
-            attend()
-
-    # host-pinned copies of the per-step inputs for the end-to-end leg
-    # The per-step inputs live as 256-byte-aligned views of one device buffer,
-    # mirrored by one pinned host buffer: the end-to-end leg moves them with a
-    # single host-to-device copy per step.
-    stage_host = stage_dev = None
+    # The end-to-end leg runs on copy 0: its per-step inputs live as
+    # 256-byte-aligned views of one device buffer, mirrored by one pinned host
+    # buffer, so that one host-to-device copy per step moves them all.
+    c0 = path.copies[0]
     if not args.no_e2e:
-        names = [("q", q), ("bt", bt), ("cl", cl)] + \
-            ([("kn", kn), ("vn", vn), ("sm", sm)] if has_append else [])
+        names = ["q", "bt", "cl"] + (["kn", "vn", "sm"] if has_append else []) + \
+            (["qstart"] if multi else []) + (["offs", "pref"] if path.groups else [])
         offs, total = [], 0
-        for _, a in names:
+        for n in names:
             offs.append(total)
-            total += (a.numel() * a.element_size() + 255) // 256 * 256
+            total += (c0[n].numel() * c0[n].element_size() + 255) // 256 * 256
         stage_dev = torch.zeros(total, dtype=torch.uint8, device=device)
         stage_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        views = {}
-        for (name, a), off in zip(names, offs):
+        for n, off in zip(names, offs):
+            a = c0[n]
             nb = a.numel() * a.element_size()
             v = stage_dev[off:off + nb].view(a.dtype).view(a.shape)
             v.copy_(a)
             stage_host[off:off + nb].copy_(a.cpu().contiguous().view(-1).view(torch.uint8))
-            views[name] = v
-        q, bt, cl = views["q"], views["bt"], views["cl"]
-        if has_append:
-            kn, vn, sm = views["kn"], views["vn"], views["sm"]
-        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            c0[n] = v
+        out_host = torch.empty(c0["out"].shape, dtype=c0["out"].dtype).pin_memory()
         h2d_bytes = total
         d2h_bytes = out_host.numel() * out_host.element_size()
 
-    def e2e_inputs():
-        stage_dev.copy_(stage_host, non_blocking=True)
-
-    # eager warm-up (also sets kernel attributes before any capture)
-    for _ in range(max(3, args.warmup)):
-        flush()
-        step()
+    # eager warm-up on every copy (also sets kernel attributes before any capture)
+    with torch.cuda.stream(timer.side):
+        for i in range(max(3, args.warmup) * ROTATE):
+            timer.flush()
+            path.step(i % ROTATE)
     torch.cuda.synchronize()
-    if pkv.get_error(err) != 0:
-        raise SystemExit(f"bench.py: device error word {pkv.get_error(err)}")
-
-    S = max(1, min(args.graph_steps, args.steps))
-    try:
-        Ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
-        Ev()
-        in_graph_events = True
-    except TypeError:
-        in_graph_events = False
-
-    def capture(body):
-        """Graph of S steps; each step = flush, then `body` between events."""
-        g = torch.cuda.CUDAGraph()
-        evs = [[Ev() for _ in range(body.n_events)] for _ in range(S)]
-        side = torch.cuda.Stream(device)
-        side.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.graph(g, stream=side):
-            for i in range(S):
-                flush()
-                body(evs[i])
-        torch.cuda.synchronize()
-        return g, evs
-
-    def step_body(ev):
-        ev[0].record()
-        step()
-        ev[1].record()
-    step_body.n_events = 2
-
-    def attn_body(ev):
-        ev[0].record()
-        attend()
-        ev[1].record()
-    attn_body.n_events = 2
-
-    def e2e_body(ev):
-        ev[0].record()
-        e2e_inputs()
-        step()
-        out_host.copy_(out, non_blocking=True)
-        ev[1].record()
-    e2e_body.n_events = 2
-
-    def timed(body, steps, eager=False):
-        """Per-step device times (ms) of each event interval over `steps` steps:
-        inside CUDA-graph replays, or around eager launches when `eager`."""
-        intervals = [[] for _ in range(body.n_events - 1)]
-        if in_graph_events and not eager:
-            g, evs = capture(body)
-            g.replay()  # one untimed replay after capture
-            torch.cuda.synchronize()
-            done = 0
-            while done < steps:
-                g.replay()
-                torch.cuda.synchronize()
-                take = min(S, steps - done)
-                for i in range(take):
-                    for k in range(body.n_events - 1):
-                        intervals[k].append(evs[i][k].elapsed_time(evs[i][k + 1]))
-                done += take
-        else:
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(body.n_events)]
-                   for _ in range(steps)]
-            for i in range(steps):
-                flush()
-                body(evs[i])
-            torch.cuda.synchronize()
-            for i in range(steps):
-                for k in range(body.n_events - 1):
-                    intervals[k].append(evs[i][k].elapsed_time(evs[i][k + 1]))
-        return intervals
-
+    if any(path.errors()):
+        raise SystemExit(f"bench.py: device error word {path.errors()}")
     # untimed graph warm-up
-    if in_graph_events:
-        timed(step_body, min(S, max(1, args.warmup)))
-        timed(attn_body, min(S, max(1, args.warmup)))
+    warm = max(1, min(args.warmup, args.graph_steps))
+    timer.back_to_back(lambda i: path.step(i % ROTATE), warm)
+    timer.isolated(lambda i: path.step(0), warm)
 
     sampler = ClockSampler(gpu_selector(torch, device))
     sampler.start()
@@ -525,87 +649,118 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    (step_ms_list,) = timed(step_body, args.steps)
+    step_ms_list = timer.back_to_back(lambda i: path.step(i % ROTATE), args.steps)
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     if world > 1:
         dist.barrier()
-    # the dominant kernel alone (paged_decode_attention), same flush discipline
-    (attn_ms,) = timed(attn_body, args.steps)
+    # the dominant call alone (paged_decode_attention), both ways
+    attn_ms = timer.back_to_back(lambda i: path.attend(i % ROTATE), args.steps)
+    step_iso = timer.isolated(lambda i: path.step(i % ROTATE), args.steps)
+    attn_iso = timer.isolated(lambda i: path.attend(i % ROTATE), args.steps)
     clocks = sampler.stop()
 
-    if pkv.get_error(err) != 0:
+    if any(path.errors()):
         raise SystemExit("bench.py: the device flagged an index error")
-    step_ms_rank = statistics.fmean(step_ms_list)
+    n_calls = args.steps
+    step_ms, value = aggregate(statistics.fmean(step_ms_list), nbytes["step"] / 1e9, world,
+                               device)
     attn_ms_mean = statistics.fmean(attn_ms)
-    step_ms, value = aggregate(step_ms_rank, nbytes["step"] / 1e9, world, device)
+    attn_iso_mean = statistics.fmean(attn_iso)
 
     # one eager-launch figure for the same step (host launch gaps included)
     eager_steps = min(args.steps, 200)
-    (eager_ms,) = timed(step_body, eager_steps, eager=True)
+    eager_ms = timer.isolated(lambda i: path.step(i % ROTATE), eager_steps, eager=True)
 
     e2e = None
     if not args.no_e2e:
-        (e2e_ms_list,) = timed(e2e_body, args.steps)
+        def e2e_body(i):
+            stage_dev.copy_(stage_host, non_blocking=True)
+            path.step(0)
+            out_host.copy_(c0["out"], non_blocking=True)
+        e2e_ms_list = timer.isolated(e2e_body, args.steps)
         e2e_ms, e2e_val = aggregate(statistics.fmean(e2e_ms_list), nbytes["step"] / 1e9, world,
                                     device)
         e2e = {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
-               "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(e2e_ms, 5)}
+               "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(e2e_ms, 5),
+               "timing": "each step its own timed region after an L2 flush: pinned-host -> "
+                         "device copy of the step's inputs, the step, device -> pinned-host "
+                         "copy of out"}
 
     layers = MODEL_LAYERS.get(args.workload, 1)
     peak, peak_src = load_peak()
     achieved = nbytes["attention"] / (attn_ms_mean * 1e-3) / 1e9
     # the committed summary covers the fp16 one-token kernel
     traffic = None if (fp8 or multi) else ncu_traffic(args.workload)
+    per_config = None
+    if rank == 0 and args.per_config and not fp8 and not multi and args.workload == WORKLOAD:
+        per_config = per_config_rows(pkv, wl, torch, device, timer, peak, args.steps,
+                                     (3, 4, 5))
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not fp8 and not multi:
         cpu = cpu_baseline(batch, args.cpu_seconds)
 
     if rank != 0:
         return
+    per_call = path.step_launches
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "steps": n_calls, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
         "config": {
             "workload": wl.WORKLOADS[args.workload], "B": B, "n_q_heads": H, "n_kv_heads": Hk,
-            "head_dim": D, "block_size": bs, "max_context_len": mcl,
+            "head_dim": D, "block_size": bs, "max_context_len": batch.max_context_len,
             "sum_context_len": int(batch.context_lens.sum()), "num_blocks": batch.num_blocks,
-            "partition_tokens": P, "step": "append + attention" if has_append else "attention",
+            "partition_tokens": path.P,
+            "step": "append + attention" if has_append else "attention",
             "bytes_per_step": nbytes["step"], "logical_bytes_per_step": nbytes["logical_step"],
-            "accumulate": "f32", "l2": "flushed before every timed step (write 2xL2, read 2xL2)",
-            "timing": "CUDA events inside CUDA-graph replays" if in_graph_events
-                      else "CUDA events around eager launches",
+            "accumulate": "f32",
+            "l2": f"inputs larger than L2: back-to-back calls cycle through {ROTATE} device "
+                  "copies of the workload's inputs (each larger than L2); the isolated "
+                  "figures flush L2 before every call (write 2xL2, read 2xL2)",
+            "timing": ("CUDA events inside CUDA-graph replays" if timer.in_graph
+                       else "CUDA events around eager launches") +
+                      f"; value, ms_per_step, attention_ms: {timer.last_s} back-to-back "
+                      "calls between two events, divided by the calls",
             "parallelism": f"replicas x{world}",
             "decode_kernel": os.environ.get("PKV_DECODE_KERNEL",
                                             "auto (tensor-core kernel when block_size % 16 == 0)"),
-            "prefix_shared": groups is not None,
+            "prefix_shared": path.groups is not None,
             "kv_dtype": "e4m3 (per-tensor scales)" if fp8 else "f16",
             "q_len": nq,
         },
         "steps_per_sec": round(1e3 / step_ms, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "attention_ms": round(attn_ms_mean, 5),
-        "percentiles_ms": {"step": pcts(step_ms_list), "attention": pcts(attn_ms)},
+        "ms_per_step_isolated": round(statistics.fmean(step_iso), 5),
+        "attention_ms_isolated": round(attn_iso_mean, 5),
+        "percentiles_ms": {"step": pcts(step_ms_list), "attention": pcts(attn_ms),
+                           "step_isolated": pcts(step_iso),
+                           "attention_isolated": pcts(attn_iso)},
         "eager_step_ms": round(statistics.fmean(eager_ms), 5),
         "model_context": {"layers": layers,
                           "model_steps_per_sec": round(1e3 / step_ms / layers, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "frac_isolated": round(nbytes["attention"] / (attn_iso_mean * 1e-3) / 1e9
+                                            / peak, 4),
                      "kernel": "paged_decode_attention: decode_balanced_kernel (one launch, "
-                               "in-kernel LSE merge)" if P == 0 else
+                               "in-kernel LSE merge)" if path.P == 0 else
                                "paged_decode_attention: partition kernel + LSE merge kernel",
+                     "timing": "achieved = attention bytes / attention_ms (back-to-back "
+                               "calls); frac_isolated uses attention_ms_isolated",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "gpu_launches_note": "per step: the append (when the step has one) and the attention "
-                             "kernel(s) -- one balanced kernel, or partition + merge kernels, or "
-                             "the shared-prefix pass + suffix pass; the attention-only timing "
-                             f"pass adds {(launches_per_step - (1 if has_append else 0)) * args.steps}"
-                             f" more, the eager pass {launches_per_step * eager_steps} more",
+        "gpu_launches": per_call * n_calls,
+        "gpu_launches_note": f"{per_call} launch(es) per step (the append when the step has "
+                             "one, then the attention: one balanced kernel, or partition + "
+                             "merge kernels, or the shared-prefix pass + suffix pass), times "
+                             "the timed steps of `value`; the other timing passes (attention "
+                             "alone, isolated calls, eager, e2e, per_config) launch more",
         "clocks": clocks,
         "wall_s_timed": round(wall1 - wall0, 3),
     }
@@ -628,12 +783,14 @@ def run_reference(args):
     # one step = a bounded sample: a few whole sequences (all heads, with append)
     per_seq = 4
     rng = np.random.default_rng(0)
+    work = (batch.k_cache.copy(), batch.v_cache.copy())
     for _ in range(max(0, args.warmup)):
-        oracle_step_sample(batch, rng.choice(batch.num_seqs, per_seq, replace=False), threads)
+        oracle_step_sample(batch, rng.choice(batch.num_seqs, per_seq, replace=False), threads,
+                           work)
     times, nb = [], []
     for _ in range(args.steps):
         dt, b = oracle_step_sample(batch, rng.choice(batch.num_seqs, per_seq, replace=False),
-                                   threads)
+                                   threads, work)
         times.append(dt)
         nb.append(b)
     total_t = sum(times)

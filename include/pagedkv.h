@@ -326,16 +326,24 @@ int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
  * GPU that loads the library holds until the process exits.  The call
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  *  - Returns PKV_ERR_WORKSPACE, launching nothing, when the problem's split
- *    needs more than PKV_NOALLOC_SCRATCH_BYTES (paged_decode_plan reports the
- *    need; a larger partition_tokens lowers it).
+ *    needs more than the array holds: more than PKV_NOALLOC_SCRATCH_BYTES
+ *    for the balanced split (partition_tokens 0, whose need paged_decode_plan
+ *    reports), or more than PKV_NOALLOC_SCRATCH_BYTES - 64 KiB for fixed
+ *    partitions (a larger partition_tokens lowers their need).
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and caches it; make that
  *    first call before any stream capture on that device.
+ *  - The array's first 64 KiB hold the balanced split's arrival counters,
+ *    which must be zero when its kernel starts.  Each balanced call clears
+ *    them on cuda_stream first (cudaMemsetAsync, which allocates nothing), so
+ *    neither a fixed-partition call nor a call that flagged
+ *    PKV_ERRBIT_TIMEOUT leaves stale counts for the next one; fixed-partition
+ *    plans keep their partial sums after those 64 KiB.  Every other byte is
+ *    written before it is read within a call.
  *  - All calls share the one array, and it keeps the last call's contents.
- *    Nothing in it needs to start at zero: each call writes every partial
- *    result it reads.  Calls whose kernels overlap in time on the GPU (on
- *    different streams, or from different host threads) race on the array
- *    and give wrong results; serialise them.
+ *    Calls whose kernels overlap in time on the GPU (on different streams,
+ *    or from different host threads) race on the array and give wrong
+ *    results; serialise them.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 int paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache,

@@ -143,19 +143,30 @@ def append(k_new, v_new, slot_mapping, k_cache, v_cache, block_size, lib=None):
     k_cache, v_cache: [NB, Hk, bs, d] fp16.  Returns (k_cache', v_cache').
     Raises OracleError when a slot lies beyond the pool.
     """
+    kc, vc = _u16(k_cache).copy(), _u16(v_cache).copy()
+    append_inplace(k_new, v_new, slot_mapping, kc, vc, block_size, lib=lib)
+    return kc.view(np.float16), vc.view(np.float16)
+
+
+def append_inplace(k_new, v_new, slot_mapping, k_cache, v_cache, block_size, lib=None):
+    """The same append, written into k_cache / v_cache themselves (contiguous
+    fp16 or uint16 arrays, modified in place)."""
     lib = lib or load()
     k_new, v_new = _u16(k_new), _u16(v_new)
-    kc, vc = _u16(k_cache).copy(), _u16(v_cache).copy()
+    for c in (k_cache, v_cache):
+        if not (isinstance(c, np.ndarray) and c.flags.c_contiguous
+                and c.dtype in (np.float16, np.uint16)):
+            raise TypeError("caches must be contiguous fp16/uint16 arrays")
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     T, Hk, d = k_new.shape
-    NB, Hk2, bs, d2 = kc.shape
-    if (Hk2, d2, bs) != (Hk, d, block_size) or v_new.shape != k_new.shape or vc.shape != kc.shape:
+    NB, Hk2, bs, d2 = k_cache.shape
+    if (Hk2, d2, bs) != (Hk, d, block_size) or v_new.shape != k_new.shape or \
+            v_cache.shape != k_cache.shape:
         raise ValueError("shape mismatch")
-    rc = lib.pkvo_append(_ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(kc), _ptr(vc), T, Hk, d,
-                         bs, NB)
+    rc = lib.pkvo_append(_ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(k_cache), _ptr(v_cache), T,
+                         Hk, d, bs, NB)
     if rc != 0:
         raise OracleError("slot beyond the pool")
-    return kc.view(np.float16), vc.view(np.float16)
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, n_q_heads, n_kv_heads,

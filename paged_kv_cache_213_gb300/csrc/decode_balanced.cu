@@ -46,7 +46,7 @@ constexpr int kWLarge = 8;
 #endif
 constexpr int kS = PKV_BAL_STAGES;  // ring stages per warp
 constexpr int kMaxSeqsBalanced = 2048;
-constexpr int kMaxWorkers = 16384;  // size of the counter region
+constexpr int kMaxWorkers = kBalancedMaxWorkers;  // size of the counter region
 constexpr int kMinUnits = 4;        // fewest units a working warp takes
 // In the suffix pass of the prefix-aware call the private parts are short
 // (forked completions: a block or two), and each output waits for the shared
@@ -78,7 +78,7 @@ struct BalCfg : MmaCfg<D> {
 __host__ __device__ constexpr size_t rec_bytes(int G, int D) {
     return (static_cast<size_t>(G) * (D + 2) * 4 + 15) / 16 * 16;
 }
-constexpr size_t kRecBase = static_cast<size_t>(kMaxWorkers) * 4;
+constexpr size_t kRecBase = kBalancedCounterBytes;
 __host__ __device__ inline size_t bal_ws_bytes(int workers, int G, int D) {
     return kRecBase + static_cast<size_t>(workers) * 2 * rec_bytes(G, D);
 }

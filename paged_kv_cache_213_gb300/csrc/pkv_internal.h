@@ -98,6 +98,13 @@ struct DecodeArgs {
     int total_q = 0;
 };
 
+// The balanced kernel's workspace starts with one int32 arrival counter per
+// worker slot, kBalancedCounterBytes in all, whatever the plan.  They must be
+// zero when a launch starts; every launch leaves them zero again unless it
+// flagged PKV_ERRBIT_TIMEOUT.
+constexpr int kBalancedMaxWorkers = 16384;
+constexpr size_t kBalancedCounterBytes = static_cast<size_t>(kBalancedMaxWorkers) * 4;
+
 // Workspace carve-up shared by the planner and the launcher.
 struct WorkspaceLayout {
     size_t acc_offset, m_offset, l_offset, total;

@@ -76,31 +76,19 @@ def oracle_f8(batch, kc8, vc8, ks, vs, mask=None):
     return dict(out=out, lse=lse, k_cache=kc8, v_cache=vc8)
 
 
-def _sample_mask(batch, n, seed):
-    rng = np.random.default_rng(seed)
-    B, H = batch.num_seqs, batch.n_q_heads
-    mask = np.zeros((B, H), dtype=bool)
-    mask.reshape(-1)[rng.choice(B * H, size=min(n, B * H), replace=False)] = True
-    mask[int(np.argmax(batch.context_lens)), :] = True
-    mask[int(np.argmin(batch.context_lens)), :] = True
-    return mask
-
-
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
 def test_fp8_workload_parity(cfg):
-    """Full-size workloads with E4M3 caches, poisoned; every output (1-3) or a
-    sample of (b, h) (4-5); the append's codes bit-exact over the whole pool."""
+    """Full-size workloads with E4M3 caches, poisoned; every output and lse
+    compared; the append's codes bit-exact over the whole pool."""
     batch = wl.workload(cfg, poison=True)
     ks, vs = _scales(batch)
     kc8, vc8 = _caches8(batch, ks, vs)
     assert np.any(kc8 == 0x7F)  # the poison became NaN codes
-    mask = None if cfg <= 3 else _sample_mask(batch, 96, cfg)
     g = gpu_f8(batch, kc8, vc8, ks, vs)
     assert g["err"] == 0
-    ref = oracle_f8(batch, kc8, vc8, ks, vs, mask=mask)
-    assert_close(g["out"], ref["out"], mask=mask, what=f"fp8 workload {cfg}")
-    sel = mask if mask is not None else np.ones(ref["lse"].shape, dtype=bool)
-    assert np.max(np.abs(g["lse"][sel] - ref["lse"][sel])) <= 1e-4
+    ref = oracle_f8(batch, kc8, vc8, ks, vs)
+    assert_close(g["out"], ref["out"], what=f"fp8 workload {cfg}")
+    assert np.max(np.abs(g["lse"] - ref["lse"])) <= 1e-4
     if batch.has_append:
         assert np.array_equal(g["k_cache"], ref["k_cache"])
         assert np.array_equal(g["v_cache"], ref["v_cache"])
