@@ -67,8 +67,11 @@ struct Plan {
     pkv::BalancedPlan bal;
 };
 
+// allow_pipeline: the balanced split may run on the producer/consumer kernel
+// (fp16 caches, no prefix groups); otherwise on per-warp ranges.
 int make_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
-              int max_blocks_per_seq, int max_context_len, int partition_tokens, Plan *plan) {
+              int max_blocks_per_seq, int max_context_len, int partition_tokens, Plan *plan,
+              bool allow_pipeline = true) {
     if (num_seqs < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
         max_blocks_per_seq <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -81,11 +84,25 @@ int make_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int blo
     if (max_len > cap) max_len = cap;
     int P = partition_tokens;
     const int group = n_q_heads / n_kv_heads;
-    if (P == 0 && pkv::kernel_override() == 0 &&
+    const int mode = pkv::kernel_override();
+    if (P == 0 && (mode == 0 || mode >= 3) &&
         pkv::balanced_supported(num_seqs, head_dim, group, block_size, 0)) {
-        // work split evenly over warps; the grid and workspace follow the device
-        if (!pkv::balanced_plan(num_seqs, n_q_heads, n_kv_heads, head_dim,
-                                static_cast<int>(max_len), &plan->bal))
+        // work split evenly over CTAs or warps; the grid and workspace follow the device.
+        // Batches of more (sequence, KV head) segments than twice the SMs
+        // (many short ones, e.g. continuous batching) run on the
+        // producer/consumer kernel, whose CTAs read every head of a block at
+        // once; fewer, longer segments run on per-warp ranges (measured on
+        // GB300: Mistral-shaped mix 50.5 -> 40.5 us; LLaMA-3-8B-shaped layer
+        // 35.0 against 36.8 us, 32k contexts 165.9 against 175.0 us).
+        const int ml = static_cast<int>(max_len);
+        int sms = 0;
+        if (sm_count(&sms) != PKV_OK) return PKV_ERR_CUDA;
+        const bool many = static_cast<long long>(num_seqs) * n_kv_heads > 2LL * sms;
+        bool done = false;
+        if (allow_pipeline && ((mode == 0 && many) || mode == 4) &&
+            pkv::pipeline_supported(num_seqs, n_kv_heads, head_dim, group, block_size, 0))
+            done = pkv::pipeline_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, ml, &plan->bal);
+        if (!done && !pkv::balanced_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, ml, &plan->bal))
             return PKV_ERR_CUDA;
         plan->balanced = true;
         plan->max_len = static_cast<int>(max_len);
@@ -263,10 +280,10 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     if (plan.balanced &&
         static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
         return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
-    const cudaError_t e =
-        plan.balanced
-            ? pkv::launch_decode_balanced(a, plan.bal, static_cast<cudaStream_t>(cuda_stream))
-            : pkv::launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    const cudaError_t e = !plan.balanced         ? pkv::launch_decode(a, stream)
+                          : plan.bal.kind == 1   ? pkv::launch_decode_pipeline(a, plan.bal, stream)
+                                                 : pkv::launch_decode_balanced(a, plan.bal, stream);
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -309,7 +326,7 @@ namespace {
 int make_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                   int max_blocks_per_seq, int max_context_len, Plan *plan) {
     int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                       max_context_len, 0, plan);
+                       max_context_len, 0, plan, false);
     if (rc != PKV_OK) return rc;
     if (!plan->balanced) return PKV_ERR_UNSUPPORTED;  // E4M3 runs on the balanced kernel only
     if (!pkv::balanced_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, plan->max_len, &plan->bal,
@@ -402,9 +419,10 @@ int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, 
                      int max_blocks_per_seq, int max_context_len, int num_groups,
                      int max_group_size, int max_prefix_len, SharedPlan *sp) {
     if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0) return PKV_ERR_INVALID_ARG;
-    if (pkv::kernel_override() != 0) return PKV_ERR_UNSUPPORTED;
+    if (pkv::kernel_override() == 1 || pkv::kernel_override() == 2) return PKV_ERR_UNSUPPORTED;
+    // the suffix pass runs on the per-warp kernel, which folds in the shared partials
     int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                       max_context_len, 0, &sp->base);
+                       max_context_len, 0, &sp->base, false);
     if (rc != PKV_OK) return rc;
     if (!sp->base.balanced) return PKV_ERR_UNSUPPORTED;
     const int g = n_q_heads / n_kv_heads;

@@ -433,6 +433,8 @@ int kernel_override() {
         const char *e = std::getenv("PKV_DECODE_KERNEL");
         if (e && std::strcmp(e, "simt") == 0) mode = 1;
         if (e && std::strcmp(e, "mma") == 0) mode = 2;
+        if (e && std::strcmp(e, "warp") == 0) mode = 3;
+        if (e && std::strcmp(e, "pipe") == 0) mode = 4;
     });
     return mode;
 }

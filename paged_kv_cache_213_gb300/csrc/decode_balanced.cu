@@ -33,6 +33,7 @@
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 #include "shared_prefix.cuh"
+#include "tile_cursor.cuh"
 
 namespace pkv {
 namespace {
@@ -92,39 +93,6 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b, bool flag
         return L < 0 ? 0 : cap;
     }
     return L;
-}
-
-// Units are ordered KV head j, then sequence b, then tile t, so that
-// sequences holding the same physical prefix blocks (forked siblings, shared
-// prompts) sit next to each other and their warps reach the shared blocks at
-// about the same time (the later reads then hit L2).  pre[] is the tile
-// prefix over sequences; TB = pre[B] units per KV head.
-struct Cursor {
-    int b, j, t;
-};
-
-__device__ __forceinline__ Cursor locate(int x, const int *pre, int B) {
-    const int TB = pre[B];
-    const int j = x / TB;
-    const int r = x - j * TB;
-    int lo = 0, hi = B - 1;  // largest b with pre[b] <= r (it has tiles)
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= r) lo = mid; else hi = mid - 1;
-    }
-    return Cursor{lo, j, r - pre[lo]};
-}
-
-__device__ __forceinline__ void advance(Cursor &c, const int *pre, int B) {
-    if (++c.t < pre[c.b + 1] - pre[c.b]) return;
-    c.t = 0;
-    do {
-        ++c.b;
-    } while (c.b < B && pre[c.b + 1] == pre[c.b]);
-    if (c.b < B) return;
-    ++c.j;
-    c.b = 0;
-    while (c.b < B && pre[c.b + 1] == pre[c.b]) ++c.b;
 }
 
 template <int D, int G, bool F8, int kW>

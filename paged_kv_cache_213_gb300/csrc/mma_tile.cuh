@@ -96,7 +96,11 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qa)[MmaCfg<D>::NP][4], co
 // columns are permuted instead of V being transposed.  Output block 4c + i,
 // column n, holds head_dim column 32c + 4n + i: o[4c + i][0] is column
 // 32c + 8tq + i and o[4c + i][1] is column 32c + 8tq + 4 + i (f8_out_col).
-template <int D, bool F8 = false>
+//
+// HS: bytes from a 64-column box of an fp16 tile to the next one (the box
+// holding columns 64 .. 127 at D = 128); MmaCfg<D>::BOX_BYTES when the tile's
+// boxes are adjacent, larger when tiles of several heads are interleaved.
+template <int D, bool F8 = false, int HS = MmaCfg<D>::BOX_BYTES>
 __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char *vs, int n_valid,
                                          const uint32_t (&qa)[MmaCfg<D>::NP][4],
                                          float scale_log2, float (&o)[MmaCfg<D>::NB_D][4],
@@ -113,7 +117,7 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
             for (int idx = lane; idx < (kMmaTile - n_valid) * per_row; idx += 32) {
                 const int r = n_valid + idx / per_row;
                 const int rem = idx % per_row;
-                *reinterpret_cast<uint4 *>(vs + (rem >> 3) * C::BOX_BYTES + r * 128 +
+                *reinterpret_cast<uint4 *>(vs + (rem >> 3) * HS + r * 128 +
                                            (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
@@ -133,7 +137,7 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
             if constexpr (F8)
                 kw = e4m3_piece<D>(ks, t, p, tq);
             else
-                kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
+                kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * HS +
                                                       swz(t, 2 * tq + (p & 1)));
             const uint32_t a0[4] = {qa[p][0], 0u, qa[p][1], 0u};
             mma_16816(sacc[nb], a0, kw.x, kw.y);
@@ -205,7 +209,7 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
         for (int qd = 0; qd < C::NB_D / 2; ++qd) {
             const int u = 2 * qd + (lm >> 1);
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
+            ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * HS + swz(vt, u & 7));
             mma_16816(o[2 * qd], pa, r0, r1);
             mma_16816(o[2 * qd + 1], pa, r2, r3);
         }

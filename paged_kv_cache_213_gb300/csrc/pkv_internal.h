@@ -122,7 +122,9 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
 // Returns cudaErrorInvalidValue for a (head_dim, group) pair with no kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 bool decode_supported(int head_dim, int group);
-// PKV_DECODE_KERNEL: 0 unset (automatic), 1 "simt", 2 "mma" (the grid kernels).
+// PKV_DECODE_KERNEL: 0 unset (automatic), 1 "simt", 2 "mma" (the grid kernels),
+// 3 "warp" (the balanced split on per-warp ranges), 4 "pipe" (the balanced
+// split on the producer/consumer kernel).
 int kernel_override();
 // Tensor-core kernel (decode_mma.cu): partition pass only, no merge.
 bool decode_mma_supported(const DecodeArgs &a);
@@ -136,9 +138,12 @@ bool make_cache_map_e4m3(CUtensorMap *m, const void *base, long long rows, int D
 // Balanced (work-split per warp) tensor-core kernel (decode_balanced.cu).
 struct BalancedPlan {
     int ctas;        // grid size
-    int warps;       // warps per CTA (4 or 8)
-    int workers;     // warps doing work = warps * ctas
+    int warps;       // warps per CTA
+    int workers;     // units of the split: warps (kind 0) or CTAs (kind 1)
     size_t ws_bytes; // workspace bytes
+    int kind = 0;    // 0: per-warp ranges (decode_balanced.cu); 1: producer/consumer
+                     // CTAs (decode_pipeline.cu)
+    int heads = 0;   // kind 1: KV heads per unit
 };
 bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
                         long long cache_rows);
@@ -147,6 +152,15 @@ bool balanced_supported(int num_seqs, int head_dim, int group, int block_size,
 bool balanced_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
                    BalancedPlan *plan, bool kv_fp8 = false);
 cudaError_t launch_decode_balanced(const DecodeArgs &a, const BalancedPlan &plan,
+                                   cudaStream_t stream);
+// The producer/consumer kernel (decode_pipeline.cu): fp16 caches, no prefix
+// groups, n_kv_heads 1, 2, 4 or a multiple of 8; a one-wave grid of CTAs,
+// each over an equal range of (head group, sequence, 16-token tile) units.
+bool pipeline_supported(int num_seqs, int n_kv_heads, int head_dim, int group, int block_size,
+                        long long cache_rows);
+bool pipeline_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
+                   BalancedPlan *plan);
+cudaError_t launch_decode_pipeline(const DecodeArgs &a, const BalancedPlan &plan,
                                    cudaStream_t stream);
 // Shared-prefix pass (decode_shared.cu): each warp holds 16 query rows.
 int shared_members_per_warp(int group);

@@ -1,7 +1,8 @@
-"""Both decode kernels stay correct: the CUDA-core kernel (the only one for
-block sizes below 16) is forced with PKV_DECODE_KERNEL=simt in a child process
-and checked against the oracle on the shapes where the tensor-core kernel is
-the default."""
+"""Every decode kernel stays correct on every shape: the CUDA-core kernel
+(the only one for block sizes below 16), the tensor-core grid kernel, and the
+balanced split on per-warp ranges or on the producer/consumer kernel are each
+forced with PKV_DECODE_KERNEL in a child process and checked against the
+oracle, also on the shapes where the automatic choice picks another one."""
 import os
 import subprocess
 import sys
@@ -26,15 +27,29 @@ for cfg in (1, 2, 3):
         assert g["err"] == 0
         ref = oracle_step(batch)
         assert_close(g["out"], ref["out"], what=f"{{cfg}} P={{P}}")
+import os
+balanced = os.environ.get("PKV_DECODE_KERNEL") in ("warp", "pipe")
 rng = np.random.default_rng(77)
 for d in (64, 128):
     for G in (1, 2, 4, 8):
         batch = wl.make_batch("v", [1, 16, 17, 200, 513], 2 * G, 2, d, 32, rng, append=True,
                               poison=True)
-        g = gpu_step(batch, partition_tokens=64)
-        assert g["err"] == 0
-        assert_close(g["out"], oracle_step(batch)["out"], what=f"d={{d}} G={{G}}")
-import os
+        for P in ((0, 64) if balanced else (64,)):
+            g = gpu_step(batch, partition_tokens=P)
+            assert g["err"] == 0
+            assert_close(g["out"], oracle_step(batch)["out"], what=f"d={{d}} G={{G}} P={{P}}")
+if balanced:
+    # the balanced split on every KV-head count it takes, ragged and empty sequences
+    for Hk in (1, 4, 8, 16):
+        for d in (64, 128):
+            lens = [0, 1, 15, 16, 17, 100, 700, 33, 2100, 64]
+            batch = wl.make_batch("h", lens, 4 * Hk, Hk, d, 16, rng, append=False, poison=True)
+            g = gpu_step(batch)
+            assert g["err"] == 0
+            ref = oracle_step(batch)
+            assert_close(g["out"], ref["out"], what=f"Hk={{Hk}} d={{d}}")
+            assert np.max(np.abs(g["lse"][1:] - ref["lse"][1:])) <= 1e-4
+            assert np.all(np.isneginf(g["lse"][0])) and not np.any(g["out"][0])
 if os.environ.get("PKV_DECODE_KERNEL") == "simt":
     from gpu_util import relayout
     base = wl.make_batch("inv", [70, 16, 530, 33], 16, 4, 128, 16, rng, append=False,
@@ -47,7 +62,7 @@ print("ok")
 """
 
 
-@pytest.mark.parametrize("kernel", ["simt", "mma"])
+@pytest.mark.parametrize("kernel", ["simt", "mma", "warp", "pipe"])
 def test_forced_kernel(kernel):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
