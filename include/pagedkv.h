@@ -216,8 +216,16 @@ int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_
  * sequences (PKV_ERR_UNSUPPORTED otherwise).  If a member's table does not
  * hold the group's first sequence's block ids for the shared prefix, that
  * member's result uses the first sequence's blocks there.
- * paged_decode_prefix_shared_plan gives the workspace bytes; the workspace
- * must be zero-filled before first use, as for the balanced split.
+ * When the groups' shared blocks take at most a quarter of the L2 cache
+ * (num_groups * max_prefix_len * n_kv_heads * head_dim * 4 bytes), or no
+ * group has two members, the call runs paged_decode_attention instead: its
+ * reads of blocks shared by several sequences then hit L2, so the shared
+ * pass would only add work.  The environment variable PKV_PREFIX_PASS=shared
+ * (or =regular), read at every call, fixes the choice.
+ * paged_decode_prefix_shared_plan gives the workspace bytes (for whichever
+ * path the call takes); the workspace must be zero-filled before first use,
+ * as for the balanced split.  pkv_bm_prefix_groups (pagedkv_blocks.h)
+ * derives the groups from the library's block manager.
  */
 int paged_decode_prefix_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                                     int block_size, int max_blocks_per_seq, int max_context_len,

@@ -93,6 +93,34 @@ int pkv_bm_block_info(const pkv_block_manager *bm, int32_t block, int32_t *refco
                       int32_t *tokens);
 
 /*
+ * Prefix groups of a batch, for paged_decode_attention_prefix_shared
+ * ("Distributed LLM Inference Serving Platform", section 2 and Lab 1:
+ * completions forked from one prompt share its blocks; section 5.1
+ * Ingestion: a cached common prefix referenced by several requests).
+ *
+ * seq_ids (host, n entries) lists the batch's sequences in row order (row b
+ * of q and of the block tables the caller passes to the attention).  The
+ * batch is cut into maximal runs of consecutive rows whose sequences hold
+ * the same physical block as their first table entry; each run is a group,
+ * and its prefix is the number of leading table entries that every member
+ * holds in common with the run's first sequence, times block_size (rows of
+ * a shared block are never written by one sharer alone: copy-on-write gives
+ * the writer its own block first).  A sequence with an empty table, or whose
+ * first block no neighbour holds, is a group of one with prefix 0.  Sharers
+ * must sit in consecutive rows to be grouped (forked siblings usually do).
+ *  group_offsets     (host) int32 [n + 1]: group i is rows
+ *                    [group_offsets[i], group_offsets[i + 1])
+ *  group_prefix_lens (host) int32 [n]: prefix tokens of group i
+ *  *num_groups, *max_group_size, *max_prefix_len  (host, may be NULL)
+ * These are the arrays and bounds the prefix-aware attention takes (copy the
+ * two arrays to the device).  PKV_ERR_INVALID_ARG on an unknown id or a null
+ * array; n == 0 gives no groups.
+ */
+int pkv_bm_prefix_groups(const pkv_block_manager *bm, const int64_t *seq_ids, int n,
+                         int32_t *group_offsets, int32_t *group_prefix_lens, int *num_groups,
+                         int *max_group_size, int *max_prefix_len);
+
+/*
  * Device block copy for copy-on-write: for each i < num_copies and every KV
  * head, rows [0, tokens[i]) of block src[i] are copied bit for bit to block
  * dst[i] in both caches (tokens == NULL: whole blocks).  src, dst, tokens are

@@ -48,6 +48,9 @@ def _lib():
         lib.pkv_bm_block_info.argtypes = [p, c.c_int32, c.POINTER(c.c_int32),
                                           c.POINTER(c.c_int32)]
         lib.pkv_bm_block_info.restype = c.c_int
+        lib.pkv_bm_prefix_groups.argtypes = [p, p, c.c_int, p, p, c.POINTER(c.c_int),
+                                             c.POINTER(c.c_int), c.POINTER(c.c_int)]
+        lib.pkv_bm_prefix_groups.restype = c.c_int
         lib.paged_kv_copy_blocks.argtypes = [p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int,
                                              c.c_int64, p, p]
         lib.paged_kv_copy_blocks.restype = c.c_int
@@ -116,6 +119,25 @@ class BlockManager:
         _check("pkv_bm_block_table", self._lib.pkv_bm_block_table(self._h, seq, buf, n.value,
                                                                   ctypes.byref(n)))
         return list(buf[: n.value])
+
+    def prefix_groups(self, seq_ids):
+        """Groups of consecutive batch rows sharing leading blocks, for
+        paged_decode_attention_prefix_shared: (offsets int32 [G+1], prefix
+        tokens int32 [G], largest group, longest prefix) as numpy arrays and
+        ints."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = int(ids.size)
+        offs = np.zeros(n + 1, dtype=np.int32)
+        pref = np.zeros(max(n, 1), dtype=np.int32)
+        g, most, longest = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check("pkv_bm_prefix_groups",
+               self._lib.pkv_bm_prefix_groups(self._h, ids.ctypes.data_as(ctypes.c_void_p), n,
+                                              offs.ctypes.data_as(ctypes.c_void_p),
+                                              pref.ctypes.data_as(ctypes.c_void_p),
+                                              ctypes.byref(g), ctypes.byref(most),
+                                              ctypes.byref(longest)))
+        return offs[: g.value + 1].copy(), pref[: g.value].copy(), most.value, longest.value
 
     def block_info(self, block: int):
         """(refcount, filled rows) of a physical block."""

@@ -6,6 +6,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "pagedkv.h"
 #include "pagedkv_blocks.h"
@@ -277,6 +279,7 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     a.partition_tokens = plan.partition;
     a.max_parts = plan.max_parts;
     a.defer_dep_wait = plan.balanced ? defer : 0;
+    a.first_wait_polls = pkv::test_wait_polls();
     if (plan.balanced &&
         static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
         return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
@@ -413,13 +416,48 @@ struct SharedPlan {
     Plan base;  // the balanced split of the private suffixes
     int chunks, parts, part_tiles, warps;
     size_t sh_acc, sh_m, sh_l, total;
+    // the shared blocks fit well inside L2: the call runs the regular
+    // attention (plan `regular`), whose reads of shared blocks hit L2 anyway
+    bool regular_path;
+    Plan regular;
 };
+
+// L2 bytes of the current device (0 when the query fails).
+long long l2_bytes() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
 
 int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                      int max_blocks_per_seq, int max_context_len, int num_groups,
                      int max_group_size, int max_prefix_len, SharedPlan *sp) {
     if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0) return PKV_ERR_INVALID_ARG;
     if (pkv::kernel_override() == 1 || pkv::kernel_override() == 2) return PKV_ERR_UNSUPPORTED;
+    // Shared prefixes that fit in a quarter of L2 are read from DRAM about
+    // once by the regular attention too (its readers of a shared block hit
+    // L2), and the regular path has no second pass to pay for: on the
+    // Mistral-shaped mix (one 512-token prefix, 2 MB) 40.5 us against 62.5 us
+    // through the two passes.  The 70B-shaped batch's prefixes (16 x 3968
+    // tokens, 260 MB) stay on the prefix-aware path.
+    const long long shared_bytes = static_cast<long long>(num_groups) * max_prefix_len *
+                                   n_kv_heads * head_dim * 2 * 2;
+    const long long l2 = l2_bytes();
+    sp->regular_path = l2 > 0 && (max_group_size < 2 || shared_bytes <= l2 / 4);
+    // PKV_PREFIX_PASS=shared / =regular fixes the choice (read at every call)
+    if (const char *e = std::getenv("PKV_PREFIX_PASS")) {
+        if (std::strcmp(e, "shared") == 0) sp->regular_path = false;
+        if (std::strcmp(e, "regular") == 0) sp->regular_path = true;
+    }
+    if (sp->regular_path) {
+        int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, max_context_len, 0, &sp->regular);
+        if (rc != PKV_OK) return rc;
+        sp->total = sp->regular.ws_bytes;
+        return PKV_OK;
+    }
     // the suffix pass runs on the per-warp kernel, which folds in the shared partials
     int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
                        max_context_len, 0, &sp->base, false);
@@ -502,6 +540,11 @@ int paged_decode_attention_prefix_shared(
         !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
         (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
         return PKV_ERR_INVALID_ARG;
+    if (sp.regular_path)
+        return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                     max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
+                                     head_dim, block_size, max_context_len, 0, workspace,
+                                     workspace_bytes, lse_out, err_word, cuda_stream, 0);
     if (!workspace || workspace_bytes < sp.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))

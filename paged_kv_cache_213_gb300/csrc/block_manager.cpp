@@ -3,6 +3,7 @@
 // of a shared partially filled tail block.  See include/pagedkv_blocks.h for
 // the page passages it follows and the reading adopted where the page's
 // listing and its worked solution disagree.
+#include <climits>
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -147,6 +148,45 @@ int pkv_bm_block_info(const pkv_block_manager *bm, int32_t block, int32_t *refco
         return PKV_ERR_INVALID_ARG;
     if (refcount) *refcount = bm->refcount[block];
     if (tokens) *tokens = bm->filled[block];
+    return PKV_OK;
+}
+
+int pkv_bm_prefix_groups(const pkv_block_manager *bm, const int64_t *seq_ids, int n,
+                         int32_t *group_offsets, int32_t *group_prefix_lens, int *num_groups,
+                         int *max_group_size, int *max_prefix_len) {
+    if (!bm || n < 0 || (n > 0 && (!seq_ids || !group_offsets || !group_prefix_lens)))
+        return PKV_ERR_INVALID_ARG;
+    std::vector<const std::vector<int32_t> *> tables(static_cast<size_t>(n));
+    for (int i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
+        tables[static_cast<size_t>(i)] = &it->second.table;
+    }
+    int groups = 0, most = 0, longest = 0;
+    if (n > 0) group_offsets[0] = 0;
+    for (int i = 0; i < n;) {
+        const std::vector<int32_t> &first = *tables[static_cast<size_t>(i)];
+        int e = i + 1;
+        size_t common = first.size();  // leading entries all members hold in common
+        while (e < n && !first.empty() && !tables[static_cast<size_t>(e)]->empty() &&
+               (*tables[static_cast<size_t>(e)])[0] == first[0]) {
+            const std::vector<int32_t> &t = *tables[static_cast<size_t>(e)];
+            size_t c = 0;
+            while (c < common && c < t.size() && t[c] == first[c]) ++c;
+            common = c;
+            ++e;
+        }
+        const long long prefix = e - i > 1 ? static_cast<long long>(common) * bm->block_size : 0;
+        const int p = prefix > INT32_MAX ? INT32_MAX : static_cast<int>(prefix);
+        group_prefix_lens[groups] = p;
+        group_offsets[++groups] = e;
+        if (e - i > most) most = e - i;
+        if (p > longest) longest = p;
+        i = e;
+    }
+    if (num_groups) *num_groups = groups;
+    if (max_group_size) *max_group_size = most;
+    if (max_prefix_len) *max_prefix_len = longest;
     return PKV_OK;
 }
 

@@ -439,6 +439,13 @@ int kernel_override() {
     return mode;
 }
 
+int test_wait_polls() {
+    const char *e = std::getenv("PKV_TEST_WAIT_POLLS");
+    if (!e || !*e) return -1;
+    const int v = std::atoi(e);
+    return v < 0 ? -1 : v;
+}
+
 bool decode_supported(int head_dim, int group) {
     return (head_dim == 64 || head_dim == 128) &&
            (group == 1 || group == 2 || group == 4 || group == 8);

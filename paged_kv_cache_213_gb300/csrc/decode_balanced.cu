@@ -504,7 +504,9 @@ __global__ void __launch_bounds__(kW * 32)
     bool timed_out = false;
     for (; k < n; ++k) {
         const int slot = k % kS;
-        const bool ok = mbar_wait_bounded(&full_bar[warp][slot], (k / kS) & 1);
+        const bool ok = (k == 0 && a.first_wait_polls >= 0)
+                            ? mbar_wait_polls(&full_bar[warp][slot], 0, a.first_wait_polls)
+                            : mbar_wait_bounded(&full_bar[warp][slot], (k / kS) & 1);
         if (__any_sync(0xffffffffu, !ok)) {
             timed_out = true;
             break;

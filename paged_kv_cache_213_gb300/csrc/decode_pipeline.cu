@@ -475,7 +475,9 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
     bool failed = false;
     for (int k = 0; k < n; ++k) {
         const int stage = k % ns;
-        const bool ok = mbar_wait_or_abort(&full_bar[stage], (k / ns) & 1, &s_abort);
+        const bool ok = (k == 0 && a.first_wait_polls >= 0)
+                            ? mbar_wait_polls(&full_bar[stage], 0, a.first_wait_polls)
+                            : mbar_wait_or_abort(&full_bar[stage], (k / ns) & 1, &s_abort);
         if (__any_sync(0xffffffffu, !ok)) {
             failed = true;
             break;

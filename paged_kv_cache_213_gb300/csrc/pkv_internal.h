@@ -96,7 +96,15 @@ struct DecodeArgs {
     // rows [query_start[b], query_start[b+1]) (its last tokens, causal)
     const int32_t *query_start = nullptr;
     int total_q = 0;
+    // Test hook (the environment variable PKV_TEST_WAIT_POLLS, read at every
+    // call): >= 0 makes each warp's first wait for K/V data give up after
+    // that many non-blocking polls, so that the timeout path (flag, drain the
+    // copies in flight, stop) runs without a fault; -1 (unset) leaves every
+    // wait at its one-second bound.
+    int first_wait_polls = -1;
 };
+// The test hook's value for this call (-1 when PKV_TEST_WAIT_POLLS is unset).
+int test_wait_polls();
 
 // The balanced kernel's workspace starts with one int32 arrival counter per
 // worker slot, kBalancedCounterBytes in all, whatever the plan.  They must be

@@ -56,6 +56,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking test of a phase (no suspension of the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// A wait that gives up after polls + 1 non-blocking tests: the test hook
+// that makes a bounded wait run out (DecodeArgs::first_wait_polls).
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t *bar, uint32_t parity, int polls) {
+    for (int i = 0; i <= polls; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    return false;
+}
+
 // Waits for the phase with the given parity to complete; false after
 // kWaitLimitNs (or kWaitLimitIters polls) without completion.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {

@@ -183,3 +183,82 @@ def test_out_of_blocks_leaves_state_unchanged(cpp):
     assert bm.num_free() == 0
     bm.free_sequence(8)
     assert bm.num_free() == 2
+
+
+def _check_groups(bm, ids, groups):
+    """The prefix groups' defining properties, checked on the block tables."""
+    offs, pref, most, longest = groups
+    tables = [bm.block_table(s) for s in ids]
+    bs = bm.block_size
+    assert offs[0] == 0 and offs[-1] == len(ids) and np.all(np.diff(offs) >= 1)
+    assert len(pref) == len(offs) - 1
+    assert most == (int(np.max(np.diff(offs))) if len(ids) else 0)
+    assert longest == (int(pref.max()) if len(pref) else 0)
+    for gi in range(len(pref)):
+        rows = list(range(offs[gi], offs[gi + 1]))
+        first = tables[rows[0]]
+        nb = int(pref[gi]) // bs
+        assert pref[gi] % bs == 0
+        if len(rows) == 1:
+            assert pref[gi] == 0
+            continue
+        # every member starts with the first member's first block ...
+        assert first and all(tables[r] and tables[r][0] == first[0] for r in rows)
+        # ... and holds its first nb blocks, and no longer common run exists
+        assert all(tables[r][:nb] == first[:nb] for r in rows)
+        assert any(len(tables[r]) <= nb or len(first) <= nb or tables[r][nb] != first[nb]
+                   for r in rows[1:])
+    # maximal runs: neighbouring groups start with different first blocks
+    for gi in range(1, len(pref)):
+        a, b = tables[offs[gi] - 1], tables[offs[gi]]
+        assert not (a and b and a[0] == b[0])
+
+
+def test_prefix_groups_properties(cpp):
+    BlockManager, _ = cpp
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        bs = int(rng.choice([1, 4, 16]))
+        bm = BlockManager(4096, bs)
+        ids, nxt = [], 0
+        for _ in range(int(rng.integers(1, 6))):  # prompts, each with forked siblings
+            root = nxt
+            nxt += 1
+            bm.add_sequence(root)
+            for _ in range(int(rng.integers(0, 70))):
+                bm.append_slot(root)
+            fam = [root]
+            for _ in range(int(rng.integers(0, 4))):
+                child = nxt
+                nxt += 1
+                bm.fork(int(rng.choice(fam)), child)
+                fam.append(child)
+            for s in fam:  # diverge by a few tokens each
+                for _ in range(int(rng.integers(0, 20))):
+                    bm.append_slot(s)
+            ids += fam
+        if trial % 3 == 0:
+            rng.shuffle(ids)  # sharers no longer adjacent: still a valid partition
+        _check_groups(bm, ids, bm.prefix_groups(ids))
+
+
+def test_prefix_groups_of_forked_prompt(cpp):
+    """Four completions forked from a 3968-token prompt, two private blocks
+    each (the 70B-shaped parallel-sampling batch): one group of four sharing
+    the prompt's 248 full blocks."""
+    BlockManager, _ = cpp
+    bm = BlockManager(2048, 16)
+    bm.add_sequence(0)
+    for _ in range(3968):
+        bm.append_slot(0)
+    for c in (1, 2, 3):
+        bm.fork(0, c)
+    for s in (0, 1, 2, 3):
+        for _ in range(32):
+            bm.append_slot(s)
+    offs, pref, most, longest = bm.prefix_groups([0, 1, 2, 3])
+    assert list(offs) == [0, 4] and list(pref) == [3968] and most == 4 and longest == 3968
+    offs, pref, _, _ = bm.prefix_groups([0, 1])
+    assert list(pref) == [3968]
+    with pytest.raises(Exception):
+        bm.prefix_groups([0, 77])  # unknown id

@@ -5,6 +5,8 @@ block manager, forked into completions that share the prompt blocks
 The cache is compared bit for bit with a CPU replay of the same copies and
 writes, and the attention with the oracle and with dense attention over the
 logical sequences."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -129,3 +131,75 @@ def test_fork_cow_decode_matches_dense():
     assert all(t[2] is None for t in toks)
     assert np.array_equal(kc.cpu().numpy().view(np.uint16), kc_cpu.view(np.uint16))
     attend()
+
+
+def test_prefix_groups_from_manager_drive_prefix_aware_attention():
+    """Parallel sampling built through the block manager (prompts prefilled,
+    forked into four completions, each decoding its own tokens with
+    copy-on-write of the shared tail), then attended through the prefix-aware
+    entry point with the groups the manager reports: equal to the oracle and
+    to the regular entry point."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rng = np.random.default_rng(5)
+    NB, bs, H, Hk, d = 1024, 16, 64, 8, 128
+    scale = 1.0 / np.sqrt(d)
+    bm = BlockManager(NB, bs)
+    kc = torch.zeros(NB, Hk, bs, d, dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+
+    def write(slots, copies):
+        if copies:
+            src = torch.tensor([c[0] for c in copies], dtype=torch.int32, device="cuda")
+            dst = torch.tensor([c[1] for c in copies], dtype=torch.int32, device="cuda")
+            rows = torch.tensor([c[2] for c in copies], dtype=torch.int32, device="cuda")
+            paged_kv_copy_blocks(kc, vc, src, dst, rows)
+        n = len(slots)
+        kn = torch.from_numpy(rng.standard_normal((n, Hk, d)).astype(np.float16)).cuda()
+        vn = torch.from_numpy(rng.standard_normal((n, Hk, d)).astype(np.float16)).cuda()
+        pkv.paged_kv_append(kn, vn, torch.tensor(slots, dtype=torch.int64, device="cuda"), kc, vc)
+
+    order = []
+    for p, L in enumerate((500, 777, 33, 260)):
+        root = 10 * p
+        bm.add_sequence(root)
+        write([bm.append_slot(root)[0] for _ in range(L)], [])
+        fam = [root] + [root + c for c in (1, 2, 3)]
+        for c in fam[1:]:
+            bm.fork(root, c)
+        for _ in range(20):  # each completion decodes its own tokens
+            slots, copies = [], []
+            for s in fam:
+                slot, copy = bm.append_slot(s)
+                slots.append(slot)
+                if copy is not None:
+                    copies.append(copy)
+            write(slots, copies)
+        order += fam
+    offs, pref, gmax, pmax = bm.prefix_groups(order)
+    assert list(np.diff(offs)) == [4, 4, 4, 4] and gmax == 4
+    assert list(pref) == [496, 768, 32, 256]  # the prompts' full blocks
+    lens = np.array([bm.length(s) for s in order], dtype=np.int32)
+    MB = max(len(bm.block_table(s)) for s in order)
+    bt = np.full((len(order), MB), -1, dtype=np.int32)
+    for i, s in enumerate(order):
+        t = bm.block_table(s)
+        bt[i, :len(t)] = t
+    q = rng.standard_normal((len(order), H, d)).astype(np.float16)
+    dq, dbt, dcl = (torch.from_numpy(x).cuda() for x in (q, bt, lens))
+    # the two-pass path (these prefixes are small enough that the library
+    # would otherwise pick the regular attention, whose L2 hits share them)
+    os.environ["PKV_PREFIX_PASS"] = "shared"
+    try:
+        shared = pkv.paged_decode_attention_prefix_shared(
+            dq, kc, vc, dbt, dcl, scale, H, Hk, d, bs, torch.from_numpy(offs).cuda(),
+            torch.from_numpy(pref).cuda(), gmax, pmax, max_context_len=int(lens.max()))
+    finally:
+        del os.environ["PKV_PREFIX_PASS"]
+    regular = pkv.paged_decode_attention(dq, kc, vc, dbt, dcl, scale, H, Hk, d, bs,
+                                         max_context_len=int(lens.max()))
+    torch.cuda.synchronize()
+    ref, _, _ = oracle.decode(q, kc.cpu().numpy(), vc.cpu().numpy(), bt, lens, scale, H, Hk, d,
+                              bs)
+    assert_close(shared.cpu().numpy(), ref, what="prefix-aware, manager groups")
+    assert_close(regular.cpu().numpy(), ref, what="regular")

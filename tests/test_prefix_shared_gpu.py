@@ -3,6 +3,8 @@ against the oracle: the Mistral-shaped mix and the 70B parallel-sampling
 workloads, and edge cases -- prefixes that are not whole tiles, members
 shorter than the prefix, sequences with no private tile, groups larger than
 one CTA chunk, one-sequence groups, every GQA group size and head_dim."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -21,7 +23,22 @@ def _cuda():
     pkv.library()
 
 
-def run_shared(batch, groups=None):
+def run_shared(batch, groups=None, pass_="shared"):
+    """The prefix-aware entry point; pass_ fixes its choice between the
+    two-pass path ("shared") and the regular attention ("regular"), or leaves
+    it to the library (None)."""
+    old_env = os.environ.pop("PKV_PREFIX_PASS", None)
+    if pass_ is not None:
+        os.environ["PKV_PREFIX_PASS"] = pass_
+    try:
+        return _run_shared(batch, groups)
+    finally:
+        os.environ.pop("PKV_PREFIX_PASS", None)
+        if old_env is not None:
+            os.environ["PKV_PREFIX_PASS"] = old_env
+
+
+def _run_shared(batch, groups=None):
     offs, pref, gmax, pmax = groups if groups is not None else wl.prefix_groups(batch)
     dev = to_dev(batch)
     if batch.has_append:
@@ -39,11 +56,13 @@ def run_shared(batch, groups=None):
     return out.cpu().numpy(), lse.cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("pass_", ["shared", None, "regular"])
 @pytest.mark.parametrize("cfg", [3, 5])
-def test_shared_workloads(cfg):
-    """Every output and lse of the full-size workload against the oracle."""
+def test_shared_workloads(cfg, pass_):
+    """Every output and lse of the full-size workload against the oracle,
+    through the two-pass path, the library's choice and the regular path."""
     batch = wl.workload(cfg, poison=True)
-    out, lse = run_shared(batch)
+    out, lse = run_shared(batch, pass_=pass_)
     ref = oracle_step(batch)
     assert_close(out, ref["out"], what=f"workload {cfg}")
     assert np.max(np.abs(lse - ref["lse"])) <= 1e-4
