@@ -127,6 +127,9 @@ __global__ void __launch_bounds__(kW * 32)
     const int bs = a.block_size;
     char *ws = reinterpret_cast<char *>(a.ws_acc);
     int *counters = reinterpret_cast<int *>(ws);
+    // the next kernel in the stream may be scheduled as this grid's CTAs
+    // retire (it waits for this grid's completion before reading anything)
+    allow_dependent_launch();
     // barriers and tensor-map prefetch first: they overlap the loads below
     if (tid == 0) {
         prefetch_tmap(&tmap_k);
@@ -136,6 +139,20 @@ __global__ void __launch_bounds__(kW * 32)
             mbar_init(&merge_bar[w], 1);
         }
         fence_barrier_init();
+    }
+    // The context lengths and block tables into L2, spread over the CTAs,
+    // while the kernel before may still be running: a prefetch cannot read
+    // stale data (L2 is where the GPU's memory is coherent), so it may come
+    // before the dependency wait; the loads after it then hit L2.
+    if (warp == 0) {
+        const size_t len_lines = (static_cast<size_t>(B) * sizeof(int32_t) + 127) / 128;
+        const size_t tab_lines =
+            (static_cast<size_t>(B) * a.max_blocks_per_seq * sizeof(int32_t) + 127) / 128;
+        for (size_t ln = static_cast<size_t>(blockIdx.x) * 32 + lane; ln < len_lines + tab_lines;
+             ln += static_cast<size_t>(gridDim.x) * 32)
+            prefetch_l2(ln < len_lines
+                            ? reinterpret_cast<const char *>(a.context_lens) + ln * 128
+                            : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
     }
     // the previous kernel in the stream (e.g. the append) is done; after the
     // shared-prefix pass, only the reads of its partials have to wait

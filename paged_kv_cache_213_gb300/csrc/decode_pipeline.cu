@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
     char *ws = reinterpret_cast<char *>(a.ws_acc);
     int *counters = reinterpret_cast<int *>(ws);
 
+    // the next kernel in the stream may be scheduled as this grid's CTAs
+    // retire (it waits for this grid's completion before reading anything)
+    allow_dependent_launch();
     if (tid == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
@@ -174,18 +177,23 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
         fence_barrier_init();
         s_abort = 0;
     }
+    // The context lengths and block tables into L2, spread over the CTAs,
+    // while the kernel before may still be running: a prefetch cannot read
+    // stale data (L2 is where the GPU's memory is coherent), so it may come
+    // before the dependency wait; the loads after it then hit L2.
+    if (warp == 0) {
+        const size_t len_lines = (static_cast<size_t>(B) * sizeof(int32_t) + 127) / 128;
+        const size_t tab_lines =
+            (static_cast<size_t>(B) * a.max_blocks_per_seq * sizeof(int32_t) + 127) / 128;
+        for (size_t ln = static_cast<size_t>(blockIdx.x) * 32 + lane; ln < len_lines + tab_lines;
+             ln += static_cast<size_t>(gridDim.x) * 32)
+            prefetch_l2(ln < len_lines
+                            ? reinterpret_cast<const char *>(a.context_lens) + ln * 128
+                            : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
+    }
     // the kernel before (e.g. the append) must be complete before anything it
     // may write is read; after this library's append only the caches are
     if (a.defer_dep_wait != 2) grid_dependency_wait();
-    // the block tables into L2, spread over the CTAs, while the lengths load:
-    // the producers' first block-id reads then hit L2
-    if (warp == 0) {
-        const size_t lines =
-            (static_cast<size_t>(B) * a.max_blocks_per_seq * sizeof(int32_t) + 127) / 128;
-        for (size_t ln = static_cast<size_t>(blockIdx.x) * 32 + lane; ln < lines;
-             ln += static_cast<size_t>(gridDim.x) * 32)
-            prefetch_l2(reinterpret_cast<const char *>(a.block_tables) + ln * 128);
-    }
 
     // --- tiles per sequence, prefix-summed: contiguous chunk per thread, then a scan
     const int chunk = (B + kThreads - 1) / kThreads;
