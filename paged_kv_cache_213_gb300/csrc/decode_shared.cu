@@ -76,18 +76,36 @@ __global__ void __launch_bounds__(kWS * 32)
     const int j = blockIdx.y;
     const int part = blockIdx.z;
     if (gi >= a.num_groups) return;
-    const int first = a.group_offsets[gi];
-    const int count = a.group_offsets[gi + 1] - first;
-    const int m0 = chunk * MPC;
-    if (count < 2 || m0 >= count) return;
-    const int nm = min(MPC, count - m0);
-
-    // shared tiles of the group (the same rule as the private-suffix kernel)
     if (tid == 0) {
         s_min_len = INT_MAX;
         for (int fb = 0; fb < kStagesS; ++fb) mbar_init(&full_bar[fb], 1);
         fence_barrier_init();
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
     }
+    // The context lengths and block tables into L2, spread over the CTAs,
+    // while the kernel before may still run (a prefetch reads nothing stale),
+    // then the wait for it before anything it may have written is read.
+    if (warp == 0) {
+        const size_t cta = blockIdx.x + static_cast<size_t>(gridDim.x) *
+                                            (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z);
+        const size_t ctas = static_cast<size_t>(gridDim.x) * gridDim.y * gridDim.z;
+        const size_t len_lines = (static_cast<size_t>(a.num_seqs) * sizeof(int32_t) + 127) / 128;
+        const size_t tab_lines =
+            (static_cast<size_t>(a.num_seqs) * a.max_blocks_per_seq * sizeof(int32_t) + 127) / 128;
+        for (size_t ln = cta * 32 + lane; ln < len_lines + tab_lines; ln += ctas * 32)
+            prefetch_l2(ln < len_lines
+                            ? reinterpret_cast<const char *>(a.context_lens) + ln * 128
+                            : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
+    }
+    grid_dependency_wait();
+    const int first = a.group_offsets[gi];
+    const int count = a.group_offsets[gi + 1] - first;
+    const int m0 = chunk * MPC;
+    if (count < 2 || m0 >= count) return;  // CTA-uniform
+    const int nm = min(MPC, count - m0);
+
+    // shared tiles of the group (the same rule as the private-suffix kernel)
     __syncthreads();
     for (int i = tid; i < count; i += nthreads) atomicMin(&s_min_len, shared_len_of(a, first + i));
     __syncthreads();
@@ -130,11 +148,8 @@ __global__ void __launch_bounds__(kWS * 32)
             }
         }
     };
-    if (tid == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
+    if (tid == 0)
         for (int i = 0; i < n && i < kStagesS; ++i) issue(i);
-    }
 
     float o[C::NB_D][4];
 #pragma unroll
@@ -205,8 +220,9 @@ cudaError_t launch_shared_t(const DecodeArgs &a, const CUtensorMap &tk, const CU
         if (e != cudaSuccess) return e;
     }
     dim3 grid(a.num_groups * a.sh_chunks, a.n_kv_heads, a.sh_parts);
-    kern<<<grid, a.sh_warps * 32, smem, stream>>>(a, tk, tv);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may start while the kernel
+    // before drains; they wait for it (griddepcontrol.wait) before reading
+    return launch_pdl(kern, grid, dim3(a.sh_warps * 32), smem, stream, a, tk, tv);
 }
 
 template <int D, int G>
