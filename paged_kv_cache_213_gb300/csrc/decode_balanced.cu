@@ -127,9 +127,6 @@ __global__ void __launch_bounds__(kW * 32)
     const int bs = a.block_size;
     char *ws = reinterpret_cast<char *>(a.ws_acc);
     int *counters = reinterpret_cast<int *>(ws);
-    // the next kernel in the stream may be scheduled as this grid's CTAs
-    // retire (it waits for this grid's completion before reading anything)
-    allow_dependent_launch();
     // barriers and tensor-map prefetch first: they overlap the loads below
     if (tid == 0) {
         prefetch_tmap(&tmap_k);
@@ -155,8 +152,14 @@ __global__ void __launch_bounds__(kW * 32)
                             : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
     }
     // the previous kernel in the stream (e.g. the append) is done; after the
-    // shared-prefix pass, only the reads of its partials have to wait
-    if (!a.defer_dep_wait) grid_dependency_wait();
+    // shared-prefix pass, only the reads of its partials have to wait.  Once
+    // this grid has waited, everything before it in the stream is complete,
+    // so the next kernel may be scheduled as this grid's CTAs retire (it too
+    // waits for this grid before reading what this grid writes).
+    if (!a.defer_dep_wait) {
+        grid_dependency_wait();
+        allow_dependent_launch();
+    }
 
     // --- tile prefix over sequences: contiguous chunk per thread, then a scan
     const int chunk = (B + kThreadsB - 1) / kThreadsB;
@@ -347,7 +350,10 @@ __global__ void __launch_bounds__(kW * 32)
         advance(pc, s_pre, B);
     };
 
-    if (a.defer_dep_wait == 2) grid_dependency_wait();  // the append has written the caches
+    if (a.defer_dep_wait == 2) {  // the append has written the caches
+        grid_dependency_wait();
+        allow_dependent_launch();
+    }
     const int pro = n < kS ? n : kS;
     for (int k = 0; k < pro; ++k) issue(k);
     int issued = pro;

@@ -163,9 +163,6 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
     char *ws = reinterpret_cast<char *>(a.ws_acc);
     int *counters = reinterpret_cast<int *>(ws);
 
-    // the next kernel in the stream may be scheduled as this grid's CTAs
-    // retire (it waits for this grid's completion before reading anything)
-    allow_dependent_launch();
     if (tid == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
@@ -192,8 +189,14 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
                             : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
     }
     // the kernel before (e.g. the append) must be complete before anything it
-    // may write is read; after this library's append only the caches are
-    if (a.defer_dep_wait != 2) grid_dependency_wait();
+    // may write is read; after this library's append only the caches are.
+    // Once this grid has waited, everything before it in the stream is
+    // complete, so the next kernel may be scheduled as this grid's CTAs
+    // retire (it too waits for this grid before reading what it writes).
+    if (a.defer_dep_wait != 2) {
+        grid_dependency_wait();
+        allow_dependent_launch();
+    }
 
     // --- tiles per sequence, prefix-summed: contiguous chunk per thread, then a scan
     const int chunk = (B + kThreads - 1) / kThreads;
@@ -261,7 +264,10 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
         int pb = seq_of(x0 % T, s_pre, B);  // its sequence
         int pt = x0 % T - s_pre[pb];        // and its tile
         int prev_key = -1;
-        if (a.defer_dep_wait == 2) grid_dependency_wait();  // the append has written the caches
+        if (a.defer_dep_wait == 2) {  // the append has written the caches
+            grid_dependency_wait();
+            allow_dependent_launch();
+        }
         int k = 0;
         bool failed = false;
         for (; k < n; ++k) {

@@ -50,9 +50,6 @@ __global__ void __launch_bounds__(kWS * 32)
                          const __grid_constant__ CUtensorMap tmap_v) {
     using C = ShCfg<D>;
     constexpr int MPW = 16 / G;  // members per warp
-    // the suffix pass that follows may be scheduled as this grid's CTAs
-    // retire: it reads nothing this kernel writes until its own dependency wait
-    allow_dependent_launch();
     const int nwarps = blockDim.x >> 5;
     const int MPC = nwarps * MPW;  // members per CTA chunk
     const int nthreads = blockDim.x;
@@ -99,6 +96,12 @@ __global__ void __launch_bounds__(kWS * 32)
                             : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
     }
     grid_dependency_wait();
+    // Everything before this grid in the stream is complete now, so the
+    // suffix pass that follows may be scheduled as this grid's CTAs retire:
+    // it reads nothing this grid writes before its own dependency wait, and
+    // what it reads before that wait (lengths, tables, the private K/V)
+    // was written before this grid started.
+    allow_dependent_launch();
     const int first = a.group_offsets[gi];
     const int count = a.group_offsets[gi + 1] - first;
     const int m0 = chunk * MPC;
