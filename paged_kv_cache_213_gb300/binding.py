@@ -493,7 +493,8 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
         _need(out, "out", torch.float16, dev)
     if ws > 0:
         if workspace is None:
-            workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+            # zero-filled: the balanced split keeps arrival counters in it
+            workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
         _need(workspace, "workspace", torch.uint8, dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)

@@ -597,6 +597,8 @@ namespace {
 struct MultiPlan {
     int max_len, partition, max_parts, row_blocks;
     size_t ws_bytes;
+    bool balanced;        // the balanced split (partition 0)
+    pkv::BalancedPlan bal;
 };
 
 int make_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads, int n_kv_heads,
@@ -616,7 +618,23 @@ int make_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads, int
     if (max_len > cap) max_len = cap;
     mp->max_len = static_cast<int>(max_len);
     mp->row_blocks = pkv::multi_row_blocks(max_q_len > 0 ? max_q_len : 1, group);
+    mp->balanced = false;
     int P = partition_tokens;
+    const int mode = pkv::kernel_override();
+    if (P == 0 && (mode == 0 || mode >= 3) &&
+        pkv::balanced_multi_supported(num_seqs, max_q_len, head_dim, group, block_size)) {
+        // every segment's query rows fit one MMA tile: the work split evenly
+        // over warps, as for decode (LLaMA-3-8B-shaped layer, 4 tokens per
+        // sequence on GB300: fixed partitions 51.4 us)
+        if (!pkv::balanced_multi_plan(num_seqs, n_q_heads, n_kv_heads, head_dim,
+                                      static_cast<int>(max_len), &mp->bal))
+            return PKV_ERR_CUDA;
+        mp->balanced = true;
+        mp->partition = 0;
+        mp->max_parts = 1;
+        mp->ws_bytes = mp->bal.ws_bytes;
+        return PKV_OK;
+    }
     if (P == 0) {
         // the largest power of two in [64, 1024] whose grid still has about
         // eight CTAs per SM (a CTA serves up to four row blocks), and at most
@@ -691,7 +709,9 @@ int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
     if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
         return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
     pkv::DecodeArgs a{};
-    if (mp.ws_bytes > 0) {
+    if (mp.balanced) {
+        a.ws_acc = static_cast<float *>(workspace);  // counters, then records
+    } else if (mp.ws_bytes > 0) {
         const pkv::WorkspaceLayout w =
             pkv::workspace_layout(total_q, n_q_heads, head_dim, mp.max_parts);
         char *base = static_cast<char *>(workspace);
@@ -720,8 +740,11 @@ int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
     a.max_parts = mp.max_parts;
     a.query_start = query_start;
     a.total_q = total_q;
-    const cudaError_t e = pkv::launch_decode_multi(a, mp.row_blocks,
-                                                   static_cast<cudaStream_t>(cuda_stream));
+    a.max_q_len = max_q_len;
+    a.first_wait_polls = pkv::test_wait_polls();
+    const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    const cudaError_t e = mp.balanced ? pkv::launch_decode_balanced_multi(a, mp.bal, stream)
+                                      : pkv::launch_decode_multi(a, mp.row_blocks, stream);
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

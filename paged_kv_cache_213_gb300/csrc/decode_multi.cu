@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(32 * kMaxMultiWarps)
     int L = a.context_lens[b];
     const long long cap_ll = static_cast<long long>(a.max_blocks_per_seq) * bs;
     const int cap = static_cast<int>(cap_ll < a.max_context_len ? cap_ll : a.max_context_len);
-    if (L < 0 || L > cap || n < 0 || n > L || q0 < 0 || q0 + n > a.total_q) {
+    if (L < 0 || L > cap || n < 0 || n > L || n > a.max_q_len || q0 < 0 || q0 + n > a.total_q) {
         if (tid == 0 && part == 0 && blockIdx.y == 0) flag_error(a.err, PKV_ERRBIT_CONTEXT);
         return;
     }
@@ -216,7 +216,10 @@ __global__ void __launch_bounds__(256) multi_merge_kernel(const DecodeArgs a) {
     const int q0 = a.query_start[b];
     const int n = a.query_start[b + 1] - q0;
     const int L = a.context_lens[b];
-    if (rq - q0 >= n || n > L || L < 0) return;  // flagged by the partition kernel
+    const long long cap_ll = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+    const int cap = static_cast<int>(cap_ll < a.max_context_len ? cap_ll : a.max_context_len);
+    // rows of a sequence the partition kernel flagged stay unwritten
+    if (rq - q0 >= n || n > L || L < 0 || L > cap || n > a.max_q_len || q0 + n > a.total_q) return;
     const int lim = L - n + (rq - q0) + 1;
     const int parts = min(a.max_parts, (lim + a.partition_tokens - 1) / a.partition_tokens);
     const size_t r0 = static_cast<size_t>(warp) * a.max_parts;

@@ -96,6 +96,7 @@ struct DecodeArgs {
     // rows [query_start[b], query_start[b+1]) (its last tokens, causal)
     const int32_t *query_start = nullptr;
     int total_q = 0;
+    int max_q_len = 0;            // host bound of n_b; a longer sequence is flagged
     // Test hook (the environment variable PKV_TEST_WAIT_POLLS, read at every
     // call): >= 0 makes each warp's first wait for K/V data give up after
     // that many non-blocking polls, so that the timeout path (flag, drain the
@@ -180,5 +181,14 @@ cudaError_t launch_decode_shared(const DecodeArgs &a, cudaStream_t stream);
 // workspace_layout(total_q, n_q_heads, head_dim, max_parts).
 int multi_row_blocks(int max_q_len, int group);
 cudaError_t launch_decode_multi(const DecodeArgs &a, int row_blocks, cudaStream_t stream);
+// Multi-token attention on the balanced split (decode_balanced_multi.cu):
+// max_q_len * group <= 16 query rows per segment, fp16 caches; workspace as
+// for the balanced decode, with 16-row records (zeroed counters first).
+bool balanced_multi_supported(int num_seqs, int max_q_len, int head_dim, int group,
+                              int block_size);
+bool balanced_multi_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
+                         BalancedPlan *plan);
+cudaError_t launch_decode_balanced_multi(const DecodeArgs &a, const BalancedPlan &plan,
+                                         cudaStream_t stream);
 
 }  // namespace pkv

@@ -113,3 +113,123 @@ def test_more_queries_than_context_is_flagged():
     batch, q, qs = _problem([5, 20], [6, 2], 8, 2, 128, 16, 9)
     out, lse, bits = _run(batch, q, qs, 6)
     assert bits & pkv.PKV_ERRBIT_CONTEXT
+
+
+# --- the balanced split (partition_tokens = 0, max_q_len * g <= 16) --------
+
+def _run_into(batch, q, qs, max_q_len, partition_tokens=0, workspace=None):
+    """The call with NaN-filled out and lse, so unwritten rows stay NaN."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    lse = torch.full((q.shape[0], batch.n_q_heads), float("nan"), device="cuda")
+    pkv.paged_decode_attention_multi(
+        _t(q), _t(batch.k_cache), _t(batch.v_cache), _t(batch.block_tables),
+        _t(batch.context_lens), _t(qs), batch.scale, batch.n_q_heads, batch.n_kv_heads,
+        batch.head_dim, batch.block_size, max_q_len, max_context_len=batch.max_context_len,
+        partition_tokens=partition_tokens, out=out, workspace=workspace, lse=lse, err_word=err)
+    bits = pkv.get_error(err)
+    return out.cpu().numpy(), lse.cpu().numpy().astype(np.float64), bits
+
+
+def _balanced(batch, qs, max_q_len):
+    P, ws = pkv.multi_plan(batch.num_seqs, int(qs[-1]), max_q_len, batch.n_q_heads,
+                           batch.n_kv_heads, batch.head_dim, batch.block_size,
+                           batch.max_blocks_per_seq, batch.max_context_len, 0)
+    return P == 0 and ws > 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_balanced_split_ragged(d, g, bs):
+    """Every (query row, head) against the oracle on the balanced split:
+    0 queries, n = L (a whole short prefill), L = 0, single tokens and the
+    most rows one segment holds (16 / g tokens), over ragged lengths; the
+    fixed-partition kernel on the same batch agrees."""
+    nmax = 16 // g
+    Hk = 2
+    lens = [1, 7, 16, 17, 40, 130, 0, 5, 300, 2, 64, 1000]
+    nq = [1, min(nmax, 7), min(nmax, 16), 0, nmax, nmax, 0, min(nmax, 5), 1, min(nmax, 2),
+          nmax, max(1, nmax - 1)]
+    batch, q, qs = _problem(lens, nq, Hk * g, Hk, d, bs, 500 + d + 10 * g + bs)
+    assert _balanced(batch, qs, nmax)
+    out, lse, bits = _run_into(batch, q, qs, nmax)
+    assert bits == 0
+    ref, ref_lse = _oracle(batch, q, qs)
+    assert_close(out, ref, what=f"balanced d={d} g={g} bs={bs}")
+    assert np.max(np.abs(lse - ref_lse)) <= 1e-4
+    out_p, _, bits_p = _run_into(batch, q, qs, nmax, partition_tokens=64)
+    assert bits_p == 0
+    assert_close(out_p, ref, what="fixed partitions")
+
+
+def test_balanced_split_many_segments():
+    """96 sequences x 8 KV heads (more segments than twice the SMs: 4-warp
+    CTAs), 4 draft tokens each over short contexts, every row checked."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(4, 700, 96)
+    batch, q, qs = _problem(lens, [4] * 96, 32, 8, 128, 16, 78)
+    assert _balanced(batch, qs, 4)
+    out, lse, bits = _run_into(batch, q, qs, 4)
+    assert bits == 0
+    ref, ref_lse = _oracle(batch, q, qs)
+    assert_close(out, ref, what="many segments")
+    assert np.max(np.abs(lse - ref_lse)) <= 1e-4
+
+
+def test_balanced_split_long_contexts_cut_segments():
+    """Few long sequences (every segment cut over many warps, merged by the
+    last arriver), 2 tokens x g = 8 rows; two calls on one workspace give
+    bit-identical results (the counters are left zero, the order is fixed)."""
+    lens = [16384, 9000, 20000, 777]
+    batch, q, qs = _problem(lens, [2, 2, 1, 2], 32, 4, 128, 16, 79)
+    P, ws = pkv.multi_plan(4, int(qs[-1]), 2, 32, 4, 128, 16, batch.max_blocks_per_seq,
+                           batch.max_context_len, 0)
+    assert P == 0
+    work = torch.zeros(ws, dtype=torch.uint8, device="cuda")
+    out1, lse1, bits1 = _run_into(batch, q, qs, 2, workspace=work)
+    out2, lse2, bits2 = _run_into(batch, q, qs, 2, workspace=work)
+    assert bits1 == 0 and bits2 == 0
+    assert np.array_equal(out1.view(np.uint16), out2.view(np.uint16))
+    assert np.array_equal(lse1, lse2)
+    ref, ref_lse = _oracle(batch, q, qs)
+    assert_close(out1, ref, what="long contexts")
+    assert np.max(np.abs(lse1 - ref_lse)) <= 1e-4
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 32])
+def test_query_count_above_max_q_len_is_flagged(partition_tokens):
+    """A sequence with more query tokens than max_q_len is flagged and its
+    rows are left unwritten; the others are computed (balanced split and
+    fixed partitions alike)."""
+    batch, q, qs = _problem([50, 80, 33], [2, 5, 1], 16, 4, 128, 16, 80)
+    out, lse, bits = _run_into(batch, q, qs, 2, partition_tokens=partition_tokens)
+    assert bits & pkv.PKV_ERRBIT_CONTEXT
+    ref, ref_lse = _oracle(batch, q, qs)
+    bad = slice(int(qs[1]), int(qs[2]))
+    assert np.isnan(out[bad].astype(np.float32)).all() and np.isnan(lse[bad]).all()
+    good = np.r_[int(qs[0]):int(qs[1]), int(qs[2]):int(qs[3])]
+    assert_close(out[good], ref[good], what="unflagged rows")
+
+
+def test_balanced_split_timeout_recovers(monkeypatch):
+    """The bounded-wait hook on the multi-token kernel: the call returns with
+    PKV_ERRBIT_TIMEOUT; after the workspace is zeroed again, a normal call
+    matches the oracle."""
+    rng = np.random.default_rng(81)
+    lens = rng.integers(100, 3000, 32)
+    batch, q, qs = _problem(lens, [4] * 32, 32, 8, 128, 16, 82)
+    P, ws = pkv.multi_plan(32, int(qs[-1]), 4, 32, 8, 128, 16, batch.max_blocks_per_seq,
+                           batch.max_context_len, 0)
+    assert P == 0
+    work = torch.zeros(ws, dtype=torch.uint8, device="cuda")
+    monkeypatch.setenv("PKV_TEST_WAIT_POLLS", "0")
+    _, _, bits = _run_into(batch, q, qs, 4, workspace=work)
+    torch.cuda.synchronize()
+    assert bits & pkv.PKV_ERRBIT_TIMEOUT and not bits & ~pkv.PKV_ERRBIT_TIMEOUT, bits
+    monkeypatch.delenv("PKV_TEST_WAIT_POLLS")
+    work.zero_()
+    out, lse, bits = _run_into(batch, q, qs, 4, workspace=work)
+    assert bits == 0
+    ref, _ = _oracle(batch, q, qs)
+    assert_close(out, ref, what="after the timeout")

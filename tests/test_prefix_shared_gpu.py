@@ -27,15 +27,15 @@ def run_shared(batch, groups=None, pass_="shared"):
     """The prefix-aware entry point; pass_ fixes its choice between the
     two-pass path ("shared") and the regular attention ("regular"), or leaves
     it to the library (None)."""
-    old_env = os.environ.pop("PKV_PREFIX_PASS", None)
+    saved = os.environ.pop("PKV_PREFIX_PASS", None)
     if pass_ is not None:
         os.environ["PKV_PREFIX_PASS"] = pass_
     try:
         return _run_shared(batch, groups)
     finally:
         os.environ.pop("PKV_PREFIX_PASS", None)
-        if old_env is not None:
-            os.environ["PKV_PREFIX_PASS"] = old_env
+        if saved is not None:
+            os.environ["PKV_PREFIX_PASS"] = saved
 
 
 def _run_shared(batch, groups=None):
@@ -110,3 +110,19 @@ def test_matches_regular_entry_point():
                                      batch.block_size, max_context_len=batch.max_context_len)
     diff = np.abs(out.astype(np.float64) - reg.cpu().numpy().astype(np.float64))
     assert diff.max() <= 2e-3
+
+
+def test_many_groups_of_forked_completions():
+    """64 prompts x 4 completions with 128-token prefixes and short private
+    suffixes (2048 grouped (sequence, KV head) segments): the two-pass path
+    and the library's choice both match the oracle."""
+    rng = np.random.default_rng(21)
+    groups = [(list(range(4 * p, 4 * p + 4)), 8) for p in range(64)]  # 128-token prefixes
+    lens = [128 + int(x) for x in rng.integers(1, 40, size=256)]
+    batch = wl.make_batch("many", lens, 16, 8, 64, 16, rng, append=False, poison=True,
+                          shared=groups)
+    ref = oracle_step(batch)
+    for pass_ in ("shared", None):
+        out, lse = run_shared(batch, pass_=pass_)
+        assert_close(out, ref["out"], what=f"pass={pass_}")
+        assert np.max(np.abs(lse - ref["lse"])) <= 1e-4
