@@ -295,16 +295,24 @@ int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
  *               tokens included (append them first); n_b <= L_b
  * Query token i of sequence b sits at position L_b - n_b + i and attends the
  * tokens [0, L_b - n_b + i] of its block table (causal); n_b = 1 is the
- * decode of paged_decode_attention.  max_q_len: host upper bound of n_b
- * (grid sizing; rows past it are not computed).  partition_tokens: KV tokens
- * per split-K partition (0 = the library's choice, else a multiple of 16 and
- * of block_size); paged_decode_multi_plan gives it and the workspace bytes
- * (0 when one partition covers max_context_len; no zero-fill needed).
+ * decode of paged_decode_attention.  max_q_len: host upper bound of n_b.
+ * partition_tokens: 0 = the library's choice, else KV tokens per split-K
+ * partition (a multiple of 16 and of block_size).  With 0, when
+ * max_q_len * (n_q_heads / n_kv_heads) <= 16 and num_seqs <= 1024, the call
+ * runs the balanced split of paged_decode_attention with every segment's
+ * query rows -- the (token, head) pairs of its n_b tokens -- in one tile: the
+ * workspace then holds arrival counters and must be zero-filled before its
+ * first use, which every call leaves zeroed (after a call that flagged
+ * PKV_ERRBIT_TIMEOUT, zero it once more).  Otherwise it runs fixed partitions,
+ * whose workspace (0 bytes when one partition covers max_context_len) needs
+ * no zero-fill.  paged_decode_multi_plan gives the partition size (0 for the
+ * balanced split) and the workspace bytes.
  * Requirements: block_size a multiple of 16, head_dim 64 or 128, n_q/n_kv in
- * {1, 2, 4, 8} (PKV_ERR_UNSUPPORTED otherwise).  A sequence with n_b > L_b or
- * rows outside [0, total_q) sets PKV_ERRBIT_CONTEXT and its rows are left
- * unwritten.  Other arguments, errors and ownership as for
- * paged_decode_attention.
+ * {1, 2, 4, 8} (PKV_ERR_UNSUPPORTED otherwise).  A sequence with n_b > L_b,
+ * n_b > max_q_len, L_b outside [0, min(max_blocks_per_seq * block_size,
+ * max_context_len)] or rows outside [0, total_q) sets PKV_ERRBIT_CONTEXT and
+ * its rows (out and lse) are left unwritten.  Other arguments, errors and
+ * ownership as for paged_decode_attention.
  */
 int paged_decode_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads,
                             int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
