@@ -205,7 +205,10 @@ def pcts(xs):
 
 def source_sha():
     h = hashlib.sha256()
-    for name in ("decode_balanced.cu", "mma_tile.cuh", "pkv_ptx.cuh", "shared_prefix.cuh"):
+    # the translation unit of the headline kernel and what it includes
+    for name in ("decode_balanced.cu", "balanced_kernel.cuh", "mma_tile.cuh",
+                 "mma_tile_multi.cuh", "pkv_ptx.cuh", "shared_prefix.cuh", "tile_cursor.cuh",
+                 "pkv_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_213_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -353,12 +356,12 @@ class Path:
         # the balanced split (P == 0) merges in-kernel; fixed partitions add a merge kernel
         self.attn_launches = 1 + (1 if self.ws_bytes > 0 and self.P > 0 else 0)
         self.groups = None
-        if prefix and batch.meta.get("shared") and not fp8 and not self.multi:
+        if prefix and batch.meta.get("shared") and not self.multi:
             offs, pref, gmax, pmax = wl.prefix_groups(batch)
             first["offs"], first["pref"] = t(offs), t(pref)
             self.groups = (gmax, pmax, len(pref))
-            self.ws_bytes = pkv.prefix_shared_plan(B, H, Hk, D, bs, MB, mcl, len(pref), gmax,
-                                                   pmax)
+            plan = pkv.prefix_shared_plan_fp8 if fp8 else pkv.prefix_shared_plan
+            self.ws_bytes = plan(B, H, Hk, D, bs, MB, mcl, len(pref), gmax, pmax)
             self.attn_launches = 2
         self.step_launches = self.attn_launches + (1 if self.has_append else 0)
         self.copies = [first] + [{k: v.clone() for k, v in first.items()}
@@ -379,6 +382,12 @@ class Path:
                                              c["qstart"], bt.scale, H, Hk, D, bs, self.nq,
                                              max_context_len=mcl, partition_tokens=self.P,
                                              out=c["out"], workspace=ws, err_word=c["err"])
+        elif self.fp8 and self.groups is not None:
+            gmax, pmax, _ = self.groups
+            pkv.paged_decode_attention_prefix_shared_fp8(
+                c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale, self.k_scale, self.v_scale,
+                H, Hk, D, bs, c["offs"], c["pref"], gmax, pmax, max_context_len=mcl,
+                out=c["out"], workspace=ws, err_word=c["err"])
         elif self.fp8:
             pkv.paged_decode_attention_fp8(c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale,
                                            self.k_scale, self.v_scale, H, Hk, D, bs,
@@ -533,41 +542,60 @@ class Timer:
         return out
 
 
-def per_config_rows(pkv, wl, torch, device, timer, peak, steps, workloads):
-    """Attention-only rows for the other standard workloads, timed like the
-    headline (both ways); the prefix-aware entry point too where the workload
-    shares prefix blocks."""
+# Rows besides the headline, timed like it: (key, workload, E4M3 caches,
+# query tokens per sequence, prefix-aware entry).
+PER_CONFIG = [
+    ("w3_regular", 3, False, 1, False), ("w3_prefix_shared", 3, False, 1, True),
+    ("w4_regular", 4, False, 1, False),
+    ("w5_regular", 5, False, 1, False), ("w5_prefix_shared", 5, False, 1, True),
+    ("w2_multi4", 2, False, 4, False),
+    ("w2_fp8", 2, True, 1, False),
+    ("w5_fp8_regular", 5, True, 1, False), ("w5_fp8_prefix_shared", 5, True, 1, True),
+]
+
+
+def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CONFIG):
+    """Attention-only rows for the other standard workloads, the prefix-aware
+    entry where a workload shares prefix blocks, 4 query tokens per sequence
+    (the multi-token call) and E4M3 caches, each timed like the headline
+    (both ways)."""
     rows = {}
-    for w in workloads:
-        batch = wl.workload(w, poison=False)
-        if batch.has_append:  # attention over the cache as generated
-            batch.slot_mapping = batch.k_new = batch.v_new = None
-        nbytes = workload_bytes(batch)["attention"]
-        variants = [("regular", False)] + ([("prefix_shared", True)]
-                                           if batch.meta.get("shared") else [])
-        for name, prefix in variants:
-            path = Path(pkv, wl, torch, batch, device, prefix=prefix)
-            for i in range(3):
-                timer.flush()
-                path.attend(i % ROTATE)
-            torch.cuda.synchronize()
-            b2b = timer.back_to_back(lambda i: path.attend(i % ROTATE), steps)
-            iso = timer.isolated(lambda i: path.attend(i % ROTATE), min(steps, 200))
-            if any(path.errors()):
-                raise SystemExit(f"bench.py: device error word on workload {w} ({name})")
-            ms, ms_iso = statistics.fmean(b2b), statistics.fmean(iso)
-            rows[f"w{w}_{name}"] = {
-                "workload": wl.WORKLOADS[w], "entry": "paged_decode_attention_prefix_shared"
-                if prefix else "paged_decode_attention",
-                "attention_bytes": nbytes, "attention_ms": round(ms, 5),
-                "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
-                "attention_ms_isolated": round(ms_iso, 5),
-                "frac_isolated": round(nbytes / (ms_iso * 1e-3) / 1e9 / peak, 4),
-                "percentiles_ms": pcts(b2b), "percentiles_ms_isolated": pcts(iso),
-                "launches_per_call": path.attn_launches,
-            }
-            del path
-            torch.cuda.empty_cache()
+    batches = {}
+    for key, w, fp8, nq, prefix in rows_spec:
+        if w not in batches:
+            batch = wl.workload(w, poison=False)
+            if batch.has_append:  # attention over the cache as generated
+                batch.slot_mapping = batch.k_new = batch.v_new = None
+            batches = {w: batch}  # one workload's arrays at a time
+        batch = batches[w]
+        nbytes = workload_bytes(batch, 1 if fp8 else 2)["attention"]
+        if nq > 1:  # the extra query rows and output rows
+            nbytes += 2 * (nq - 1) * batch.num_seqs * batch.n_q_heads * batch.head_dim * 2
+        path = Path(pkv, wl, torch, batch, device, fp8=fp8, q_len=nq, prefix=prefix)
+        for i in range(3):
+            timer.flush()
+            path.attend(i % ROTATE)
+        torch.cuda.synchronize()
+        b2b = timer.back_to_back(lambda i: path.attend(i % ROTATE), steps)
+        iso = timer.isolated(lambda i: path.attend(i % ROTATE), min(steps, 200))
+        if any(path.errors()):
+            raise SystemExit(f"bench.py: device error word on row {key}")
+        ms, ms_iso = statistics.fmean(b2b), statistics.fmean(iso)
+        entry = ("paged_decode_attention_multi" if nq > 1 else
+                 "paged_decode_attention" + ("_prefix_shared" if prefix else "") +
+                 ("_fp8" if fp8 else ""))
+        rows[key] = {
+            "workload": wl.WORKLOADS[w], "entry": entry,
+            "kv_dtype": "e4m3" if fp8 else "f16", "query_tokens_per_seq": nq,
+            "attention_bytes": nbytes, "attention_ms": round(ms, 5),
+            "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
+            "attention_ms_isolated": round(ms_iso, 5),
+            "frac_isolated": round(nbytes / (ms_iso * 1e-3) / 1e9 / peak, 4),
+            "percentiles_ms": pcts(b2b), "percentiles_ms_isolated": pcts(iso),
+            "launches_per_call": path.attn_launches,
+        }
+        del path
+        torch.cuda.empty_cache()
     return rows
 
 
@@ -694,8 +722,7 @@ def run_ours(args):
     traffic = None if (fp8 or multi) else ncu_traffic(args.workload)
     per_config = None
     if rank == 0 and args.per_config and not fp8 and not multi and args.workload == WORKLOAD:
-        per_config = per_config_rows(pkv, wl, torch, device, timer, peak, args.steps,
-                                     (3, 4, 5))
+        per_config = per_config_rows(pkv, wl, torch, device, timer, peak, args.steps)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not fp8 and not multi:
         cpu = cpu_baseline(batch, args.cpu_seconds)

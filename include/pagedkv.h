@@ -281,6 +281,33 @@ int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
                                float *lse_out, int32_t *err_word, void *cuda_stream);
 
 /*
+ * Prefix-aware decode attention over E4M3 caches: paged_decode_attention_
+ * prefix_shared with the caches, scales and results of
+ * paged_decode_attention_fp8 (same reading of the FP8 format and scales; the
+ * KV-cache list of "Roadmap: vLLM-style serving features for TornadoVM
+ * batched decode" together with section 2 of "Distributed LLM Inference
+ * Serving Platform").  The shared pass reads each shared E4M3 tile once per
+ * chunk of members and widens it in the tile math.  The L2 rule counts one
+ * byte per value (num_groups * max_prefix_len * n_kv_heads * head_dim * 2
+ * bytes); below it, or with no group of two, the call runs
+ * paged_decode_attention_fp8.  paged_decode_prefix_shared_plan_fp8 gives the
+ * workspace bytes; the workspace must be zero-filled before its first use.
+ * Groups, arguments, requirements and errors as for the two calls above.
+ */
+int paged_decode_prefix_shared_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads,
+                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                        int max_context_len, int num_groups, int max_group_size,
+                                        int max_prefix_len, size_t *workspace_bytes_out);
+int paged_decode_attention_prefix_shared_fp8(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, float k_scale, float v_scale,
+    int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
+    const int32_t *group_offsets, const int32_t *group_prefix_lens, int num_groups,
+    int max_group_size, int max_prefix_len, void *workspace, size_t workspace_bytes,
+    float *lse_out, int32_t *err_word, void *cuda_stream);
+
+/*
  * Multi-token (causal) paged attention: several new tokens of each sequence
  * attend in one call -- verifying speculative draft tokens, or a chunk of a
  * chunked prefill ("Roadmap: vLLM-style serving features for TornadoVM

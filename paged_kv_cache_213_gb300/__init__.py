@@ -23,9 +23,11 @@ from .binding import (  # noqa: F401
     paged_decode_attention_fp8,
     paged_decode_attention_multi,
     paged_decode_attention_prefix_shared,
+    paged_decode_attention_prefix_shared_fp8,
     paged_kv_append,
     paged_kv_append_fp8,
     paged_decode_step,
     prefix_shared_plan,
+    prefix_shared_plan_fp8,
     status_string,
 )

@@ -263,19 +263,92 @@ def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
 
 
-def prefix_shared_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                       max_context_len, num_groups, max_group_size, max_prefix_len):
-    """Workspace bytes of paged_decode_attention_prefix_shared."""
+def _prefix_shared_plan(name, num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                        max_blocks_per_seq, max_context_len, num_groups, max_group_size,
+                        max_prefix_len):
     lib = library()
-    fn = lib.paged_decode_prefix_shared_plan
+    fn = getattr(lib, name)
     c = ctypes
     fn.argtypes = [c.c_int] * 10 + [c.POINTER(c.c_size_t)]
     fn.restype = c.c_int
     W = c.c_size_t(0)
-    _check("paged_decode_prefix_shared_plan",
-           fn(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
-              max_context_len, num_groups, max_group_size, max_prefix_len, c.byref(W)))
+    _check(name, fn(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                    max_context_len, num_groups, max_group_size, max_prefix_len, c.byref(W)))
     return W.value
+
+
+def prefix_shared_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                       max_context_len, num_groups, max_group_size, max_prefix_len):
+    """Workspace bytes of paged_decode_attention_prefix_shared."""
+    return _prefix_shared_plan("paged_decode_prefix_shared_plan", num_seqs, n_q_heads,
+                               n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                               max_context_len, num_groups, max_group_size, max_prefix_len)
+
+
+def prefix_shared_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, max_context_len, num_groups, max_group_size,
+                           max_prefix_len):
+    """Workspace bytes of paged_decode_attention_prefix_shared_fp8."""
+    return _prefix_shared_plan("paged_decode_prefix_shared_plan_fp8", num_seqs, n_q_heads,
+                               n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                               max_context_len, num_groups, max_group_size, max_prefix_len)
+
+
+def _prefix_shared_call(scales, q, k_cache, v_cache, block_tables, context_lens, scale,
+                        n_q_heads, n_kv_heads, head_dim, block_size, group_offsets,
+                        group_prefix_lens, max_group_size, max_prefix_len, max_context_len, out,
+                        workspace, lse, err_word):
+    """scales: None (fp16 caches) or (k_scale, v_scale) of E4M3 caches."""
+    fp8 = scales is not None
+    name = "paged_decode_attention_prefix_shared" + ("_fp8" if fp8 else "")
+    lib = library()
+    fn = getattr(lib, name)
+    c = ctypes
+    p = c.c_void_p
+    fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float] + \
+        ([c.c_float, c.c_float] if fp8 else []) + \
+        [c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, p, c.c_int, c.c_int, c.c_int, p,
+         c.c_size_t, p, p, p]
+    fn.restype = c.c_int
+    dev = q.device
+    kv_dtype = torch.uint8 if fp8 else torch.float16
+    for t, nm, dt in ((q, "q", torch.float16), (k_cache, "k_cache", kv_dtype),
+                      (v_cache, "v_cache", kv_dtype),
+                      (block_tables, "block_tables", torch.int32),
+                      (context_lens, "context_lens", torch.int32),
+                      (group_offsets, "group_offsets", torch.int32),
+                      (group_prefix_lens, "group_prefix_lens", torch.int32)):
+        _need(t, nm, dt, dev)
+    B, MB = block_tables.shape
+    G = group_prefix_lens.numel()
+    if group_offsets.numel() != G + 1:
+        raise ValueError("group_offsets must have num_groups + 1 entries")
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    ws = _prefix_shared_plan("paged_decode_prefix_shared_plan" + ("_fp8" if fp8 else ""), B,
+                             n_q_heads, n_kv_heads, head_dim, block_size, MB, mcl, G,
+                             max_group_size, max_prefix_len)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, dev)
+    if workspace is None:
+        # zero-filled: the balanced split keeps arrival counters in it
+        workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    extra = [float(scales[0]), float(scales[1])] if fp8 else []
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), *extra, n_q_heads,
+                n_kv_heads, head_dim, block_size, mcl, _ptr(group_offsets),
+                _ptr(group_prefix_lens), G, int(max_group_size), int(max_prefix_len),
+                _ptr(workspace), workspace.numel(), _ptr(lse), _ptr(err_word),
+                _stream_handle(dev))
+    _check(name, rc)
+    return out
 
 
 def paged_decode_attention_prefix_shared(q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -286,47 +359,24 @@ def paged_decode_attention_prefix_shared(q, k_cache, v_cache, block_tables, cont
     """Decode attention that reads each group's shared prefix blocks once per
     chunk of members.  group_offsets [G+1] and group_prefix_lens [G] are int32
     CUDA tensors (consecutive ranges of sequences, shared prefix tokens)."""
-    lib = library()
-    fn = lib.paged_decode_attention_prefix_shared
-    c = ctypes
-    p = c.c_void_p
-    fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float, c.c_int, c.c_int,
-                   c.c_int, c.c_int, c.c_int, p, p, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p,
-                   p, p]
-    fn.restype = c.c_int
-    dev = q.device
-    for t, name, dt in ((q, "q", torch.float16), (k_cache, "k_cache", torch.float16),
-                        (v_cache, "v_cache", torch.float16),
-                        (block_tables, "block_tables", torch.int32),
-                        (context_lens, "context_lens", torch.int32),
-                        (group_offsets, "group_offsets", torch.int32),
-                        (group_prefix_lens, "group_prefix_lens", torch.int32)):
-        _need(t, name, dt, dev)
-    B, MB = block_tables.shape
-    G = group_prefix_lens.numel()
-    if group_offsets.numel() != G + 1:
-        raise ValueError("group_offsets must have num_groups + 1 entries")
-    mcl = 0 if max_context_len is None else int(max_context_len)
-    ws = prefix_shared_plan(B, n_q_heads, n_kv_heads, head_dim, block_size, MB, mcl, G,
-                            max_group_size, max_prefix_len)
-    if out is None:
-        out = torch.empty_like(q)
-    if workspace is None:
-        # zero-filled: the balanced split keeps arrival counters in it
-        workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
-    _need(workspace, "workspace", torch.uint8, dev)
-    if lse is not None:
-        _need(lse, "lse", torch.float32, dev)
-    if err_word is not None:
-        _need(err_word, "err_word", torch.int32, dev)
-    with torch.cuda.device(dev):
-        rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), n_q_heads, n_kv_heads,
-                head_dim, block_size, mcl, _ptr(group_offsets), _ptr(group_prefix_lens), G,
-                int(max_group_size), int(max_prefix_len), _ptr(workspace), workspace.numel(),
-                _ptr(lse), _ptr(err_word), _stream_handle(dev))
-    _check("paged_decode_attention_prefix_shared", rc)
-    return out
+    return _prefix_shared_call(None, q, k_cache, v_cache, block_tables, context_lens, scale,
+                               n_q_heads, n_kv_heads, head_dim, block_size, group_offsets,
+                               group_prefix_lens, max_group_size, max_prefix_len,
+                               max_context_len, out, workspace, lse, err_word)
+
+
+def paged_decode_attention_prefix_shared_fp8(q, k_cache, v_cache, block_tables, context_lens,
+                                             scale, k_scale, v_scale, n_q_heads, n_kv_heads,
+                                             head_dim, block_size, group_offsets,
+                                             group_prefix_lens, max_group_size, max_prefix_len,
+                                             max_context_len=None, out=None, workspace=None,
+                                             lse=None, err_word=None):
+    """The prefix-aware call over E4M3 caches (uint8 codes; values code *
+    k_scale and code * v_scale)."""
+    return _prefix_shared_call((k_scale, v_scale), q, k_cache, v_cache, block_tables,
+                               context_lens, scale, n_q_heads, n_kv_heads, head_dim, block_size,
+                               group_offsets, group_prefix_lens, max_group_size, max_prefix_len,
+                               max_context_len, out, workspace, lse, err_word)
 
 
 # ---------------------------------------------------------------------------

@@ -431,9 +431,10 @@ long long l2_bytes() {
     return n;
 }
 
+// fp8: E4M3 caches (one byte per value; both passes widen in the tile math).
 int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                      int max_blocks_per_seq, int max_context_len, int num_groups,
-                     int max_group_size, int max_prefix_len, SharedPlan *sp) {
+                     int max_group_size, int max_prefix_len, SharedPlan *sp, bool fp8 = false) {
     if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0) return PKV_ERR_INVALID_ARG;
     if (pkv::kernel_override() == 1 || pkv::kernel_override() == 2) return PKV_ERR_UNSUPPORTED;
     // Shared prefixes that fit in a quarter of L2 are read from DRAM about
@@ -443,7 +444,7 @@ int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, 
     // through the two passes.  The 70B-shaped batch's prefixes (16 x 3968
     // tokens, 260 MB) stay on the prefix-aware path.
     const long long shared_bytes = static_cast<long long>(num_groups) * max_prefix_len *
-                                   n_kv_heads * head_dim * 2 * 2;
+                                   n_kv_heads * head_dim * 2 * (fp8 ? 1 : 2);
     const long long l2 = l2_bytes();
     sp->regular_path = l2 > 0 && (max_group_size < 2 || shared_bytes <= l2 / 4);
     // PKV_PREFIX_PASS=shared / =regular fixes the choice (read at every call)
@@ -452,15 +453,19 @@ int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, 
         if (std::strcmp(e, "regular") == 0) sp->regular_path = true;
     }
     if (sp->regular_path) {
-        int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
-                           max_blocks_per_seq, max_context_len, 0, &sp->regular);
+        int rc = fp8 ? make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                     max_blocks_per_seq, max_context_len, &sp->regular)
+                     : make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                 max_blocks_per_seq, max_context_len, 0, &sp->regular);
         if (rc != PKV_OK) return rc;
         sp->total = sp->regular.ws_bytes;
         return PKV_OK;
     }
     // the suffix pass runs on the per-warp kernel, which folds in the shared partials
-    int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                       max_context_len, 0, &sp->base, false);
+    int rc = fp8 ? make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                 max_blocks_per_seq, max_context_len, &sp->base)
+                 : make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, max_context_len, 0, &sp->base, false);
     if (rc != PKV_OK) return rc;
     if (!sp->base.balanced) return PKV_ERR_UNSUPPORTED;
     const int g = n_q_heads / n_kv_heads;
@@ -475,7 +480,7 @@ int make_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, 
     int sms = 0;
     rc = sm_count(&sms);
     if (rc != PKV_OK) return rc;
-    const int per_sm = pkv::shared_ctas_per_sm(head_dim, g, sp->warps);
+    const int per_sm = pkv::shared_ctas_per_sm(head_dim, g, sp->warps, fp8);
     if (per_sm <= 0) return PKV_ERR_CUDA;
     // one wave of CTAs over the (group chunk, KV head) pairs, at least 4 tiles each
     const long long pairs =
@@ -516,22 +521,43 @@ int paged_decode_prefix_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads,
     return rc;
 }
 
-int paged_decode_attention_prefix_shared(
-    void *out, const void *q, const void *k_cache, const void *v_cache,
-    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
-    int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads, int n_kv_heads,
-    int head_dim, int block_size, int max_context_len, const int32_t *group_offsets,
-    const int32_t *group_prefix_lens, int num_groups, int max_group_size, int max_prefix_len,
-    void *workspace, size_t workspace_bytes, float *lse_out, int32_t *err_word,
-    void *cuda_stream) {
+int paged_decode_prefix_shared_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads,
+                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                        int max_context_len, int num_groups, int max_group_size,
+                                        int max_prefix_len, size_t *workspace_bytes_out) {
+    SharedPlan sp{};
+    const int rc = make_shared_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                    max_blocks_per_seq, max_context_len, num_groups,
+                                    max_group_size, max_prefix_len, &sp, true);
+    if (rc == PKV_OK && workspace_bytes_out) *workspace_bytes_out = sp.total;
+    return rc;
+}
+
+}  // extern "C"
+
+namespace {
+
+// paged_decode_attention_prefix_shared(_fp8): fp8 selects E4M3 caches with
+// scales k_scale, v_scale (1, 1 for fp16).
+int prefix_shared_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                       int max_blocks_per_seq, int64_t num_blocks, float scale, float k_scale,
+                       float v_scale, bool fp8, int n_q_heads, int n_kv_heads, int head_dim,
+                       int block_size, int max_context_len, const int32_t *group_offsets,
+                       const int32_t *group_prefix_lens, int num_groups, int max_group_size,
+                       int max_prefix_len, void *workspace, size_t workspace_bytes,
+                       float *lse_out, int32_t *err_word, void *cuda_stream) {
     if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
+                !(v_scale > 0.f)))
+        return PKV_ERR_INVALID_ARG;
     if (num_groups > 0 && (!group_offsets || !group_prefix_lens || !aligned(group_offsets, 4) ||
                            !aligned(group_prefix_lens, 4)))
         return PKV_ERR_INVALID_ARG;
     SharedPlan sp{};
     int rc = make_shared_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
                               max_blocks_per_seq, max_context_len, num_groups, max_group_size,
-                              max_prefix_len, &sp);
+                              max_prefix_len, &sp, fp8);
     if (rc != PKV_OK) return rc;
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -541,10 +567,17 @@ int paged_decode_attention_prefix_shared(
         (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
         return PKV_ERR_INVALID_ARG;
     if (sp.regular_path)
-        return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                                     max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
-                                     head_dim, block_size, max_context_len, 0, workspace,
-                                     workspace_bytes, lse_out, err_word, cuda_stream, 0);
+        return fp8 ? paged_decode_attention_fp8(out, q, k_cache, v_cache, block_tables,
+                                                context_lens, num_seqs, max_blocks_per_seq,
+                                                num_blocks, scale, k_scale, v_scale, n_q_heads,
+                                                n_kv_heads, head_dim, block_size,
+                                                max_context_len, workspace, workspace_bytes,
+                                                lse_out, err_word, cuda_stream)
+                   : decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens,
+                                           num_seqs, max_blocks_per_seq, num_blocks, scale,
+                                           n_q_heads, n_kv_heads, head_dim, block_size,
+                                           max_context_len, 0, workspace, workspace_bytes,
+                                           lse_out, err_word, cuda_stream, 0);
     if (!workspace || workspace_bytes < sp.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
@@ -563,7 +596,11 @@ int paged_decode_attention_prefix_shared(
     a.num_seqs = num_seqs;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    // E4M3 keys: q . (code * k_scale) * scale; outputs times v_scale
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.f) *
+                                      1.4426950408889634);
+    a.kv_fp8 = fp8 ? 1 : 0;
+    a.v_scale = fp8 ? v_scale : 1.f;
     a.n_q_heads = n_q_heads;
     a.n_kv_heads = n_kv_heads;
     a.head_dim = head_dim;
@@ -582,12 +619,48 @@ int paged_decode_attention_prefix_shared(
     a.sh_m = reinterpret_cast<float *>(base + sp.sh_m);
     a.sh_l = reinterpret_cast<float *>(base + sp.sh_l);
     a.defer_dep_wait = num_groups > 0 ? 1 : 0;  // the shared pass runs just before
+    a.first_wait_polls = pkv::test_wait_polls();
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e = cudaSuccess;
     if (num_groups > 0) e = pkv::launch_decode_shared(a, stream);
     if (e == cudaSuccess) e = pkv::launch_decode_balanced(a, sp.base.bal, stream);
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_decode_attention_prefix_shared(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads, int n_kv_heads,
+    int head_dim, int block_size, int max_context_len, const int32_t *group_offsets,
+    const int32_t *group_prefix_lens, int num_groups, int max_group_size, int max_prefix_len,
+    void *workspace, size_t workspace_bytes, float *lse_out, int32_t *err_word,
+    void *cuda_stream) {
+    return prefix_shared_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              max_blocks_per_seq, num_blocks, scale, 1.f, 1.f, false, n_q_heads,
+                              n_kv_heads, head_dim, block_size, max_context_len, group_offsets,
+                              group_prefix_lens, num_groups, max_group_size, max_prefix_len,
+                              workspace, workspace_bytes, lse_out, err_word, cuda_stream);
+}
+
+int paged_decode_attention_prefix_shared_fp8(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, float k_scale, float v_scale,
+    int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
+    const int32_t *group_offsets, const int32_t *group_prefix_lens, int num_groups,
+    int max_group_size, int max_prefix_len, void *workspace, size_t workspace_bytes,
+    float *lse_out, int32_t *err_word, void *cuda_stream) {
+    return prefix_shared_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              max_blocks_per_seq, num_blocks, scale, k_scale, v_scale, true,
+                              n_q_heads, n_kv_heads, head_dim, block_size, max_context_len,
+                              group_offsets, group_prefix_lens, num_groups, max_group_size,
+                              max_prefix_len, workspace, workspace_bytes, lse_out, err_word,
+                              cuda_stream);
 }
 
 }  // extern "C"

@@ -278,8 +278,10 @@ __global__ void __launch_bounds__(kW * 32)
     __syncthreads();
 
     // Sequences without private tiles (sequences spread over the CTAs): empty
-    // ones get out = 0, lse = -inf; the others are the shared pass's result.
-    // (Multi-token: a sequence without tiles has no query rows, or is flagged.)
+    // ones get out = 0, lse = -inf; the others are the shared pass's result
+    // (E4M3: its partial sums are in the tile math's register order, in units
+    // of v_scale).  (Multi-token: a sequence without tiles has no query rows,
+    // or is flagged.)
     for (int b = blockIdx.x; !MT && b < B; b += gridDim.x) {
         if (s_pre[b + 1] != s_pre[b]) continue;
         grid_dependency_wait();  // the shared pass's partials are complete
@@ -295,10 +297,10 @@ __global__ void __launch_bounds__(kW * 32)
                     if (mp == -INFINITY) continue;
                     const float wgt = exp2f(mp - M);
                     Ls = fmaf(wgt, a.sh_l[r0 + pp], Ls);
-                    A = fmaf(wgt, a.sh_acc[(r0 + pp) * D + i % D], A);
+                    A = fmaf(wgt, a.sh_acc[(r0 + pp) * D + (F8 ? f8_acc_index(i % D) : i % D)], A);
                 }
             }
-            ob[i] = __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
+            ob[i] = __float2half_rn(Ls > 0.f ? A * a.v_scale / Ls : 0.f);
             if (a.lse_out && i % D == 0)
                 a.lse_out[static_cast<size_t>(b) * H + h] = Ls > 0.f ? (M + log2f(Ls)) * kLn2b : -INFINITY;
         }
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kW * 32)
     auto write_out = [&](int b, int j, float fm, float fl) {
         if (g >= G) return;
         const size_t bh = static_cast<size_t>(b) * H + static_cast<size_t>(j) * G + g;
-        if (!F8 && s_skip[b] > 0) {  // fold in the shared-prefix partial states
+        if (s_skip[b] > 0) {  // fold in the shared-prefix partial states (same register order)
             grid_dependency_wait();  // complete and visible once the shared pass is done
             const size_t r0 = bh * a.sh_parts;
             float M = fm;

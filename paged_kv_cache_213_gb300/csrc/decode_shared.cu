@@ -15,7 +15,11 @@
 // blocks shared by parallel completions with a reference count) and Lab 1
 // (forkSequence); attention per sections 3 and 5.1 of that page; the split
 // of one softmax into partial states merged by log-sum-exp follows
-// FlashAttention-2 (section 14 references).
+// FlashAttention-2 (section 14 references).  E4M3 caches ("Roadmap:
+// vLLM-style serving features for TornadoVM batched decode", KV-cache list:
+// quantized FP8 KV cache) are widened in the tile math; their partial sums
+// keep the E4M3 tile math's register order and v_scale units, as the suffix
+// pass expects.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -37,18 +41,20 @@ constexpr int kWS = 4;  // most warps per CTA (the launch uses only those with r
 #endif
 constexpr int kStagesS = PKV_SHARED_STAGES;  // CTA-wide ring
 
-template <int D>
+template <int D, bool F8>
 struct ShCfg : MmaCfg<D> {
-    static constexpr int STAGE_BYTES = 2 * MmaCfg<D>::TILE_BYTES;
+    // one tile of one cache: fp16 TMA boxes, or one box of E4M3 codes
+    static constexpr int KV_BYTES = F8 ? kMmaTile * D : MmaCfg<D>::TILE_BYTES;
+    static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // multiple of 1024
     static constexpr int PIPE_BYTES = kStagesS * STAGE_BYTES;
 };
 
-template <int D, int G>
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kWS * 32)
     decode_shared_kernel(const __grid_constant__ DecodeArgs a,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v) {
-    using C = ShCfg<D>;
+    using C = ShCfg<D, F8>;
     constexpr int MPW = 16 / G;  // members per warp
     const int nwarps = blockDim.x >> 5;
     const int MPC = nwarps * MPW;  // members per CTA chunk
@@ -139,15 +145,20 @@ __global__ void __launch_bounds__(kWS * 32)
         const bool ok = id >= 0 && id < a.num_blocks;
         if (!ok) flag_error(a.err, PKV_ERRBIT_BLOCK_ID);
         s_ok[st] = ok;
-        mbar_arrive_expect_tx(&full_bar[st], ok ? 2 * C::TILE_BYTES : 0);
+        mbar_arrive_expect_tx(&full_bar[st], ok ? 2 * C::KV_BYTES : 0);
         if (ok) {
             unsigned char *kdst = smem + st * C::STAGE_BYTES;
-            unsigned char *vdst = kdst + C::TILE_BYTES;
+            unsigned char *vdst = kdst + C::KV_BYTES;
             const int row = (id * Hk + j) * bs + (tok0 % bs);
+            if constexpr (F8) {  // one swizzled box per cache
+                tma_load_2d(kdst, &tmap_k, 0, row, &full_bar[st]);
+                tma_load_2d(vdst, &tmap_v, 0, row, &full_bar[st]);
+            } else {
 #pragma unroll
-            for (int bx = 0; bx < C::BOXES; ++bx) {
-                tma_load_2d(kdst + bx * C::BOX_BYTES, &tmap_k, bx * 64, row, &full_bar[st]);
-                tma_load_2d(vdst + bx * C::BOX_BYTES, &tmap_v, bx * 64, row, &full_bar[st]);
+                for (int bx = 0; bx < C::BOXES; ++bx) {
+                    tma_load_2d(kdst + bx * C::BOX_BYTES, &tmap_k, bx * 64, row, &full_bar[st]);
+                    tma_load_2d(vdst + bx * C::BOX_BYTES, &tmap_v, bx * 64, row, &full_bar[st]);
+                }
             }
         }
     };
@@ -169,8 +180,8 @@ __global__ void __launch_bounds__(kWS * 32)
         }
         if (s_ok[st]) {  // a bad block id leaves this tile out (flagged above)
             const unsigned char *ks = smem + st * C::STAGE_BYTES;
-            mma_tile_2rows<D>(ks, ks + C::TILE_BYTES, qlo, qhi, a.scale_log2, o, m_lo, l_lo, m_hi,
-                              l_hi, lane);
+            mma_tile_2rows<D, F8>(ks, ks + C::KV_BYTES, qlo, qhi, a.scale_log2, o, m_lo, l_lo,
+                                  m_hi, l_hi, lane);
         }
         __syncthreads();  // every warp is done with stage st
         if (tid == 0 && i + kStagesS < n) issue(i + kStagesS);
@@ -211,12 +222,12 @@ __global__ void __launch_bounds__(kWS * 32)
     }
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t launch_shared_t(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t stream) {
-    using C = ShCfg<D>;
+    using C = ShCfg<D, F8>;
     const size_t smem = 1024 + C::PIPE_BYTES;
-    auto kern = decode_shared_kernel<D, G>;
+    auto kern = decode_shared_kernel<D, G, F8>;
     if (smem > 48 * 1024) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -228,10 +239,10 @@ cudaError_t launch_shared_t(const DecodeArgs &a, const CUtensorMap &tk, const CU
     return launch_pdl(kern, grid, dim3(a.sh_warps * 32), smem, stream, a, tk, tv);
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 int shared_ctas_per_sm_t(int warps) {
-    using C = ShCfg<D>;
-    auto kern = decode_shared_kernel<D, G>;
+    using C = ShCfg<D, F8>;
+    auto kern = decode_shared_kernel<D, G, F8>;
     const size_t smem = 1024 + C::PIPE_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -247,9 +258,11 @@ int shared_ctas_per_sm_t(int warps) {
 int shared_members_per_warp(int group) { return 16 / group; }
 int shared_max_warps() { return kWS; }
 
-int shared_ctas_per_sm(int head_dim, int group, int warps) {
-#define PKV_SH_OCC(D_, G_) \
-    if (head_dim == D_ && group == G_) return shared_ctas_per_sm_t<D_, G_>(warps);
+int shared_ctas_per_sm(int head_dim, int group, int warps, bool kv_fp8) {
+#define PKV_SH_OCC(D_, G_)                                                               \
+    if (head_dim == D_ && group == G_)                                                     \
+        return kv_fp8 ? shared_ctas_per_sm_t<D_, G_, true>(warps)                          \
+                      : shared_ctas_per_sm_t<D_, G_, false>(warps);
     PKV_SH_OCC(128, 1)
     PKV_SH_OCC(128, 2)
     PKV_SH_OCC(128, 4)
@@ -265,12 +278,16 @@ int shared_ctas_per_sm(int head_dim, int group, int warps) {
 cudaError_t launch_decode_shared(const DecodeArgs &a, cudaStream_t stream) {
     const long long rows = a.num_blocks * a.n_kv_heads * static_cast<long long>(a.block_size);
     CUtensorMap tk, tv;
-    if (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
-        !make_cache_map(&tv, a.v_cache, rows, a.head_dim))
+    if (a.kv_fp8 ? (!make_cache_map_e4m3(&tk, a.k_cache, rows, a.head_dim) ||
+                    !make_cache_map_e4m3(&tv, a.v_cache, rows, a.head_dim))
+                 : (!make_cache_map(&tk, a.k_cache, rows, a.head_dim) ||
+                    !make_cache_map(&tv, a.v_cache, rows, a.head_dim)))
         return cudaErrorNotSupported;
     const int g = a.n_q_heads / a.n_kv_heads;
-#define PKV_SH_CASE(D_, G_) \
-    if (a.head_dim == D_ && g == G_) return launch_shared_t<D_, G_>(a, tk, tv, stream);
+#define PKV_SH_CASE(D_, G_)                                                         \
+    if (a.head_dim == D_ && g == G_)                                                 \
+        return a.kv_fp8 ? launch_shared_t<D_, G_, true>(a, tk, tv, stream)           \
+                        : launch_shared_t<D_, G_, false>(a, tk, tv, stream);
     PKV_SH_CASE(128, 1)
     PKV_SH_CASE(128, 2)
     PKV_SH_CASE(128, 4)

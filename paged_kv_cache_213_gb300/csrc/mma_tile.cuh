@@ -85,6 +85,41 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qa)[MmaCfg<D>::NP][4], co
     }
 }
 
+// Where head_dim column `col` sits in a row of partial sums stored in
+// register order (float2 number 4 * nb + tq holds o[nb][0], o[nb][1] of lane
+// 4g + tq) by the E4M3 tile math: column 32c + 8tq + e is o[4c + e % 4][e / 4].
+__host__ __device__ __forceinline__ int f8_acc_index(int col) {
+    const int c = col >> 5, tq = (col >> 3) & 3, e = col & 7;
+    return 2 * ((4 * c + (e & 3)) * 4 + tq) + (e >> 2);
+}
+
+// O += P V for an E4M3 V tile (D-byte swizzle): lane 4g + tq loads the
+// 4-byte words at column 32c + 4g of rows 2tq, 2tq+1, 2tq+8, 2tq+9 and pairs
+// their bytes, so byte i of each row pair feeds output block 4c + i, column g
+// (the permuted column order described at mma_tile).  pa: the A fragment of P.
+template <int D>
+__device__ __forceinline__ void pv_e4m3(const unsigned char *vs, const uint32_t (&pa)[4],
+                                        float (&o)[MmaCfg<D>::NB_D][4], int lane) {
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        const int wc = 8 * c + g;  // 4-byte word of the row
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq, wc));
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 1, wc));
+        const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 8, wc));
+        const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 9, wc));
+        const uint32_t lo01 = __byte_perm(w0, w1, 0x5140);  // byte 0 pair, byte 1 pair
+        const uint32_t lo23 = __byte_perm(w0, w1, 0x7362);  // byte 2 pair, byte 3 pair
+        const uint32_t hi01 = __byte_perm(w2, w3, 0x5140);
+        const uint32_t hi23 = __byte_perm(w2, w3, 0x7362);
+        mma_16816(o[4 * c + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(hi01));
+        mma_16816(o[4 * c + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
+        mma_16816(o[4 * c + 2], pa, e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(hi23));
+        mma_16816(o[4 * c + 3], pa, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+    }
+}
+
 // One tile: rows [0, n_valid) of the K tile `ks` and V tile `vs` take part;
 // the V rows past n_valid are zeroed first (they may hold another sequence's
 // data or NaN and must not reach P.V).  Updates the running state of head g.
@@ -95,7 +130,7 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qa)[MmaCfg<D>::NP][4], co
 // 4-byte words of those four rows and pairs their bytes, so the output
 // columns are permuted instead of V being transposed.  Output block 4c + i,
 // column n, holds head_dim column 32c + 4n + i: o[4c + i][0] is column
-// 32c + 8tq + i and o[4c + i][1] is column 32c + 8tq + 4 + i (f8_out_col).
+// 32c + 8tq + i and o[4c + i][1] is column 32c + 8tq + 4 + i (f8_acc_index).
 //
 // HS: bytes from a 64-column box of an fp16 tile to the next one (the box
 // holding columns 64 .. 127 at D = 128); MmaCfg<D>::BOX_BYTES when the tile's
@@ -179,27 +214,7 @@ __device__ __forceinline__ void mma_tile(const unsigned char *ks, unsigned char 
     const uint32_t pa[4] = {pack_half2(pv[0][0], pv[0][1]), 0u, pack_half2(pv[1][0], pv[1][1]),
                             0u};
     if constexpr (F8) {
-        // O += P V, E4M3 V: words of rows 2tq, 2tq+1, 2tq+8, 2tq+9 at column
-        // 32c + 4g; byte i of each row pair is output block 4c + i, column g
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            const int wc = 8 * c + g;  // 4-byte word of the row
-            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq, wc));
-            const uint32_t w1 =
-                *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 1, wc));
-            const uint32_t w2 =
-                *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 8, wc));
-            const uint32_t w3 =
-                *reinterpret_cast<const uint32_t *>(vs + e4m3_word_off<D>(2 * tq + 9, wc));
-            const uint32_t lo01 = __byte_perm(w0, w1, 0x5140);  // byte 0 pair, byte 1 pair
-            const uint32_t lo23 = __byte_perm(w0, w1, 0x7362);  // byte 2 pair, byte 3 pair
-            const uint32_t hi01 = __byte_perm(w2, w3, 0x5140);
-            const uint32_t hi23 = __byte_perm(w2, w3, 0x7362);
-            mma_16816(o[4 * c + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(hi01));
-            mma_16816(o[4 * c + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
-            mma_16816(o[4 * c + 2], pa, e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(hi23));
-            mma_16816(o[4 * c + 3], pa, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
-        }
+        pv_e4m3<D>(vs, pa, o, lane);
     } else {
         // O += P V: V fragments by transposed 8x8 loads, two 8-column blocks per load
         const int lm = lane >> 3;
@@ -224,7 +239,8 @@ namespace pkv {
 // ("hi") of lane 4g+tq, each with its own online-softmax state.  Used where
 // one K/V tile serves several sequences' queries at once (shared prefixes).
 // All 16 rows of the tile take part (a shared prefix is made of full tiles).
-template <int D>
+// F8: E4M3 tiles as in mma_tile, with the same permuted output columns.
+template <int D, bool F8 = false>
 __device__ __forceinline__ void mma_tile_2rows(const unsigned char *ks, const unsigned char *vs,
                                                const uint32_t (&qlo)[MmaCfg<D>::NP][4],
                                                const uint32_t (&qhi)[MmaCfg<D>::NP][4],
@@ -241,8 +257,12 @@ __device__ __forceinline__ void mma_tile_2rows(const unsigned char *ks, const un
         const int t = nb * 8 + g;
 #pragma unroll
         for (int p = 0; p < C::NP; ++p) {
-            const uint4 kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
-                                                              swz(t, 2 * tq + (p & 1)));
+            uint4 kw;
+            if constexpr (F8)
+                kw = e4m3_piece<D>(ks, t, p, tq);
+            else
+                kw = *reinterpret_cast<const uint4 *>(ks + (p >> 1) * C::BOX_BYTES +
+                                                      swz(t, 2 * tq + (p & 1)));
             const uint32_t a0[4] = {qlo[p][0], qhi[p][0], qlo[p][1], qhi[p][1]};
             mma_16816(sacc[nb], a0, kw.x, kw.y);
             const uint32_t a1[4] = {qlo[p][2], qhi[p][2], qlo[p][3], qhi[p][3]};
@@ -291,16 +311,20 @@ __device__ __forceinline__ void mma_tile_2rows(const unsigned char *ks, const un
     }
     const uint32_t pa[4] = {pack_half2(pl[0][0], pl[0][1]), pack_half2(ph[0][0], ph[0][1]),
                             pack_half2(pl[1][0], pl[1][1]), pack_half2(ph[1][0], ph[1][1])};
-    const int lm = lane >> 3;
-    const int ri = lane & 7;
-    const int vt = ((lm & 1) << 3) + ri;
+    if constexpr (F8) {
+        pv_e4m3<D>(vs, pa, o, lane);
+    } else {
+        const int lm = lane >> 3;
+        const int ri = lane & 7;
+        const int vt = ((lm & 1) << 3) + ri;
 #pragma unroll
-    for (int qd = 0; qd < C::NB_D / 2; ++qd) {
-        const int u = 2 * qd + (lm >> 1);
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
-        mma_16816(o[2 * qd], pa, r0, r1);
-        mma_16816(o[2 * qd + 1], pa, r2, r3);
+        for (int qd = 0; qd < C::NB_D / 2; ++qd) {
+            const int u = 2 * qd + (lm >> 1);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(r0, r1, r2, r3, vs + (u >> 3) * C::BOX_BYTES + swz(vt, u & 7));
+            mma_16816(o[2 * qd], pa, r0, r1);
+            mma_16816(o[2 * qd + 1], pa, r2, r3);
+        }
     }
 }
 

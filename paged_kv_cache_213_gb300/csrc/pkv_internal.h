@@ -174,7 +174,7 @@ cudaError_t launch_decode_pipeline(const DecodeArgs &a, const BalancedPlan &plan
 // Shared-prefix pass (decode_shared.cu): each warp holds 16 query rows.
 int shared_members_per_warp(int group);
 int shared_max_warps();
-int shared_ctas_per_sm(int head_dim, int group, int warps);
+int shared_ctas_per_sm(int head_dim, int group, int warps, bool kv_fp8 = false);
 cudaError_t launch_decode_shared(const DecodeArgs &a, cudaStream_t stream);
 // Multi-token causal attention (decode_multi.cu): grid (max_parts, Hk x row
 // blocks, B) plus the merge kernel when max_parts > 1; workspace as

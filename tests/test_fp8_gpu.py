@@ -178,3 +178,75 @@ def test_fp8_host_rejections():
             _t(oracle.quantize_e4m3(b8.v_cache, vs)), _t(b8.block_tables),
             _t(b8.context_lens), b8.scale, ks, vs, 8, 2, 128, 8)
     assert e.value.status == -2
+
+
+# --- the prefix-aware call over E4M3 caches --------------------------------
+
+def gpu_f8_shared(batch, kc8, vc8, ks, vs, groups=None, pass_="shared"):
+    """Append (if any) then paged_decode_attention_prefix_shared_fp8; pass_
+    fixes the two-pass path ("shared"), or leaves the choice to the library
+    (None)."""
+    import os
+    offs, pref, gmax, pmax = groups if groups is not None else wl.prefix_groups(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kc, vc = _t(kc8), _t(vc8)
+    if batch.has_append:
+        pkv.paged_kv_append_fp8(_t(batch.k_new), _t(batch.v_new), _t(batch.slot_mapping), kc, vc,
+                                ks, vs, err_word=err)
+    lse = torch.full((batch.num_seqs, batch.n_q_heads), float("nan"), device="cuda")
+    saved = os.environ.pop("PKV_PREFIX_PASS", None)
+    if pass_ is not None:
+        os.environ["PKV_PREFIX_PASS"] = pass_
+    try:
+        out = pkv.paged_decode_attention_prefix_shared_fp8(
+            _t(batch.q), kc, vc, _t(batch.block_tables), _t(batch.context_lens), batch.scale, ks,
+            vs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size, _t(offs),
+            _t(pref), gmax, pmax, max_context_len=batch.max_context_len, lse=lse, err_word=err)
+    finally:
+        os.environ.pop("PKV_PREFIX_PASS", None)
+        if saved is not None:
+            os.environ["PKV_PREFIX_PASS"] = saved
+    bits = pkv.get_error(err)
+    return out.cpu().numpy(), lse.cpu().numpy().astype(np.float64), bits
+
+
+@pytest.mark.parametrize("pass_", ["shared", None])
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_fp8_prefix_shared_workloads(cfg, pass_):
+    """Full-size shared-prefix workloads with E4M3 caches, poisoned: every
+    output and lse of the prefix-aware call against the oracle's E4M3 decode,
+    through the two-pass path and the library's choice."""
+    batch = wl.workload(cfg, poison=True)
+    ks, vs = _scales(batch)
+    kc8, vc8 = _caches8(batch, ks, vs)
+    out, lse, bits = gpu_f8_shared(batch, kc8, vc8, ks, vs, pass_=pass_)
+    assert bits == 0
+    ref = oracle_f8(batch, kc8, vc8, ks, vs)
+    assert_close(out, ref["out"], what=f"fp8 prefix-aware workload {cfg}")
+    assert np.max(np.abs(lse - ref["lse"])) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_fp8_prefix_shared_edge_cases(d, g):
+    """Groups of 5 (one member shorter than the prefix), 2 (no private tile:
+    the output is the shared pass's alone, its columns mapped back from the
+    E4M3 tile math's order), 1, and 3 with a prefix that is no whole tile."""
+    rng = np.random.default_rng(900 + 10 * d + g)
+    Hk = 2
+    lens = [100, 60, 33, 130, 75, 64, 64, 40, 90, 91, 70]
+    shared = [([0, 1, 2, 3, 4], 3), ([5, 6], 4), ([8, 9, 10], 3)]
+    batch = wl.make_batch("f8edge", lens, Hk * g, Hk, d, 16, rng, append=False, poison=True,
+                          shared=shared)
+    groups = (np.array([0, 5, 7, 8, 11], dtype=np.int32), np.array([48, 64, 0, 37], dtype=np.int32),
+              5, 64)
+    ks, vs = _scales(batch)
+    kc8, vc8 = _caches8(batch, ks, vs)
+    out, lse, bits = gpu_f8_shared(batch, kc8, vc8, ks, vs, groups)
+    assert bits == 0
+    ref = oracle_f8(batch, kc8, vc8, ks, vs)
+    assert_close(out, ref["out"], what=f"fp8 prefix-aware d={d} g={g}")
+    assert np.max(np.abs(lse - ref["lse"])) <= 1e-4
+    # the regular E4M3 call on the same caches agrees
+    reg = gpu_f8(batch, kc8, vc8, ks, vs)
+    assert np.max(np.abs(out.astype(np.float64) - reg["out"].astype(np.float64))) <= 2e-3
