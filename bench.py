@@ -554,6 +554,29 @@ PER_CONFIG = [
 ]
 
 
+def kernel_label(path, torch, device):
+    """The entry point and kernel(s) the attention call of `path` runs (the
+    library's dispatch rule, restated for the label only)."""
+    bt = path.batch
+    if path.multi:
+        return ("paged_decode_attention_multi: decode_balanced_kernel with multi-token rows "
+                "(one launch)" if path.P == 0 else
+                "paged_decode_attention_multi: decode_multi_kernel + multi_merge_kernel")
+    if path.groups is not None:
+        return ("paged_decode_attention_prefix_shared" + ("_fp8" if path.fp8 else "") +
+                ": decode_shared_kernel (shared pass) + decode_balanced_kernel (suffix pass), "
+                "or the regular call when the shared blocks fit in L2")
+    if path.fp8:
+        return "paged_decode_attention_fp8: decode_balanced_kernel on E4M3 tiles (one launch)"
+    if path.P != 0:
+        return "paged_decode_attention: partition kernel + LSE merge kernel"
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    if bt.num_seqs * bt.n_kv_heads > 2 * sms and not os.environ.get("PKV_DECODE_KERNEL"):
+        return ("paged_decode_attention: decode_pipeline_kernel (producer/consumer CTAs, one "
+                "launch, in-kernel LSE merge)")
+    return "paged_decode_attention: decode_balanced_kernel (one launch, in-kernel LSE merge)"
+
+
 def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CONFIG):
     """Attention-only rows for the other standard workloads, the prefix-aware
     entry where a workload shares prefix blocks, 4 query tokens per sequence
@@ -772,9 +795,7 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "frac_isolated": round(nbytes["attention"] / (attn_iso_mean * 1e-3) / 1e9
                                             / peak, 4),
-                     "kernel": "paged_decode_attention: decode_balanced_kernel (one launch, "
-                               "in-kernel LSE merge)" if path.P == 0 else
-                               "paged_decode_attention: partition kernel + LSE merge kernel",
+                     "kernel": kernel_label(path, torch, device),
                      "timing": "achieved = attention bytes / attention_ms (back-to-back "
                                "calls); frac_isolated uses attention_ms_isolated",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"

@@ -36,17 +36,23 @@ namespace pkv {
 namespace {
 
 constexpr int kWS = 4;  // most warps per CTA (the launch uses only those with rows)
+// Stages of the CTA-wide ring: fp16 tiles; E4M3 tiles (half the bytes, so
+// twice the stages keep as many bytes in flight: 70B-shaped batch, E4M3,
+// with the suffix pass: 78.5 us at 4 stages, about 71 at 8).
 #ifndef PKV_SHARED_STAGES
 #define PKV_SHARED_STAGES 4
 #endif
-constexpr int kStagesS = PKV_SHARED_STAGES;  // CTA-wide ring
+#ifndef PKV_SHARED_STAGES_F8
+#define PKV_SHARED_STAGES_F8 8
+#endif
 
 template <int D, bool F8>
 struct ShCfg : MmaCfg<D> {
+    static constexpr int STAGES = F8 ? PKV_SHARED_STAGES_F8 : PKV_SHARED_STAGES;
     // one tile of one cache: fp16 TMA boxes, or one box of E4M3 codes
     static constexpr int KV_BYTES = F8 ? kMmaTile * D : MmaCfg<D>::TILE_BYTES;
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // multiple of 1024
-    static constexpr int PIPE_BYTES = kStagesS * STAGE_BYTES;
+    static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
 };
 
 template <int D, int G, bool F8>
@@ -55,6 +61,7 @@ __global__ void __launch_bounds__(kWS * 32)
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v) {
     using C = ShCfg<D, F8>;
+    constexpr int kStagesS = C::STAGES;
     constexpr int MPW = 16 / G;  // members per warp
     const int nwarps = blockDim.x >> 5;
     const int MPC = nwarps * MPW;  // members per CTA chunk
