@@ -364,6 +364,9 @@ class Path:
             self.ws_bytes = plan(B, H, Hk, D, bs, MB, mcl, len(pref), gmax, pmax)
             self.attn_launches = 2
         self.step_launches = self.attn_launches + (1 if self.has_append else 0)
+        # launch flags of the plain fp16 attention call (PKV_TABLES_READY where
+        # the caller knows that the kernel before writes no lengths or tables)
+        self.attn_flags = 0
         self.copies = [first] + [{k: v.clone() for k, v in first.items()}
                                  for _ in range(copies - 1)]
         for c in self.copies:
@@ -398,11 +401,17 @@ class Path:
             pkv.paged_decode_attention_prefix_shared(
                 c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale, H, Hk, D, bs, c["offs"],
                 c["pref"], gmax, pmax, max_context_len=mcl, out=c["out"], workspace=ws,
-                err_word=c["err"])
+                err_word=c["err"], flags=self.attn_flags)
         else:
             pkv.paged_decode_attention(c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale, H,
                                        Hk, D, bs, max_context_len=mcl, partition_tokens=self.P,
-                                       out=c["out"], workspace=ws, err_word=c["err"])
+                                       out=c["out"], workspace=ws, err_word=c["err"],
+                                       flags=self.attn_flags)
+
+    def flaggable(self):
+        """The attention call is a plain or prefix-aware fp16 one, which take
+        launch flags."""
+        return not (self.multi or self.fp8)
 
     def step(self, i):
         """append + attention: one library call when the step has an append on
@@ -563,7 +572,8 @@ def kernel_label(path, torch, device):
                 "(one launch)" if path.P == 0 else
                 "paged_decode_attention_multi: decode_multi_kernel + multi_merge_kernel")
     if path.groups is not None:
-        return ("paged_decode_attention_prefix_shared" + ("_fp8" if path.fp8 else "") +
+        return ("paged_decode_attention_prefix_shared" +
+                ("_fp8" if path.fp8 else "_ex (PKV_TABLES_READY)") +
                 ": decode_shared_kernel (shared pass) + decode_balanced_kernel (suffix pass), "
                 "or the regular call when the shared blocks fit in L2")
     if path.fp8:
@@ -572,9 +582,10 @@ def kernel_label(path, torch, device):
         return "paged_decode_attention: partition kernel + LSE merge kernel"
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     if bt.num_seqs * bt.n_kv_heads > 2 * sms and not os.environ.get("PKV_DECODE_KERNEL"):
-        return ("paged_decode_attention: decode_pipeline_kernel (producer/consumer CTAs, one "
-                "launch, in-kernel LSE merge)")
-    return "paged_decode_attention: decode_balanced_kernel (one launch, in-kernel LSE merge)"
+        return ("paged_decode_attention_ex (PKV_TABLES_READY): decode_pipeline_kernel "
+                "(producer/consumer CTAs, one launch, in-kernel LSE merge)")
+    return ("paged_decode_attention_ex (PKV_TABLES_READY): decode_balanced_kernel (one launch, "
+            "in-kernel LSE merge)")
 
 
 def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CONFIG):
@@ -599,14 +610,20 @@ def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CO
             timer.flush()
             path.attend(i % ROTATE)
         torch.cuda.synchronize()
+        plain = None
+        if path.flaggable():  # as the headline: flagged back to back, plain too
+            plain = timer.back_to_back(lambda i: path.attend(i % ROTATE), steps)
+            path.attn_flags = pkv.PKV_TABLES_READY
         b2b = timer.back_to_back(lambda i: path.attend(i % ROTATE), steps)
+        path.attn_flags = 0
         iso = timer.isolated(lambda i: path.attend(i % ROTATE), min(steps, 200))
         if any(path.errors()):
             raise SystemExit(f"bench.py: device error word on row {key}")
         ms, ms_iso = statistics.fmean(b2b), statistics.fmean(iso)
         entry = ("paged_decode_attention_multi" if nq > 1 else
                  "paged_decode_attention" + ("_prefix_shared" if prefix else "") +
-                 ("_fp8" if fp8 else ""))
+                 ("_fp8" if fp8 else "") +
+                 ("_ex (PKV_TABLES_READY)" if plain is not None else ""))
         rows[key] = {
             "workload": wl.WORKLOADS[w], "entry": entry,
             "kv_dtype": "e4m3" if fp8 else "f16", "query_tokens_per_seq": nq,
@@ -616,7 +633,12 @@ def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CO
             "frac_isolated": round(nbytes / (ms_iso * 1e-3) / 1e9 / peak, 4),
             "percentiles_ms": pcts(b2b), "percentiles_ms_isolated": pcts(iso),
             "launches_per_call": path.attn_launches,
+            "flags": "PKV_TABLES_READY" if plain is not None else "none",
         }
+        if plain is not None:
+            mp = statistics.fmean(plain)
+            rows[key]["attention_ms_plain_call"] = round(mp, 5)
+            rows[key]["frac_plain_call"] = round(nbytes / (mp * 1e-3) / 1e9 / peak, 4)
         del path
         torch.cuda.empty_cache()
     return rows
@@ -705,8 +727,17 @@ def run_ours(args):
     wall1 = time.perf_counter()
     if world > 1:
         dist.barrier()
-    # the dominant call alone (paged_decode_attention), both ways
+    # the dominant call alone, both ways.  Back to back, each call is made as
+    # in a decode loop whose tables are copied in before the layers run: the
+    # kernel before it (the previous call) writes no lengths or tables, so the
+    # plain fp16 call takes PKV_TABLES_READY; the same calls without the flag
+    # are timed too (attention_ms_plain_call).
+    attn_plain = None
+    if path.flaggable():
+        attn_plain = timer.back_to_back(lambda i: path.attend(i % ROTATE), args.steps)
+        path.attn_flags = pkv.PKV_TABLES_READY
     attn_ms = timer.back_to_back(lambda i: path.attend(i % ROTATE), args.steps)
+    path.attn_flags = 0
     step_iso = timer.isolated(lambda i: path.step(i % ROTATE), args.steps)
     attn_iso = timer.isolated(lambda i: path.attend(i % ROTATE), args.steps)
     clocks = sampler.stop()
@@ -783,6 +814,9 @@ def run_ours(args):
         "steps_per_sec": round(1e3 / step_ms, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "attention_ms": round(attn_ms_mean, 5),
+        "attention_flags": "PKV_TABLES_READY" if attn_plain is not None else "none",
+        "attention_ms_plain_call": round(statistics.fmean(attn_plain), 5)
+        if attn_plain is not None else None,
         "ms_per_step_isolated": round(statistics.fmean(step_iso), 5),
         "attention_ms_isolated": round(attn_iso_mean, 5),
         "percentiles_ms": {"step": pcts(step_ms_list), "attention": pcts(attn_ms),
@@ -795,9 +829,14 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "frac_isolated": round(nbytes["attention"] / (attn_iso_mean * 1e-3) / 1e9
                                             / peak, 4),
+                     "frac_plain_call": round(nbytes["attention"] /
+                                              (statistics.fmean(attn_plain) * 1e-3) / 1e9 / peak,
+                                              4) if attn_plain is not None else None,
                      "kernel": kernel_label(path, torch, device),
                      "timing": "achieved = attention bytes / attention_ms (back-to-back "
-                               "calls); frac_isolated uses attention_ms_isolated",
+                               "calls, PKV_TABLES_READY on the plain fp16 call); "
+                               "frac_plain_call: the same calls without the flag; "
+                               "frac_isolated uses attention_ms_isolated",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "per_config": per_config,

@@ -170,6 +170,32 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int32_t *err_word, void *cuda_stream);
 
 /*
+ * paged_decode_attention with launch flags.  The pages have no counterpart:
+ * this is how the call overlaps the kernel before it on the stream.
+ *  PKV_TABLES_READY  the caller guarantees that the kernel launched just
+ *                    before this call on cuda_stream (if any) writes neither
+ *                    context_lens nor block_tables -- in a decode loop the
+ *                    tables are copied in before the layers run, and the
+ *                    kernel before the attention writes q and the caches.
+ *                    The call then reads the lengths and block ids and
+ *                    plans its work split while that kernel drains
+ *                    (programmatic dependent launch), and waits for it only
+ *                    before it reads q, the caches or the workspace.  If the
+ *                    guarantee does not hold, the results are unspecified.
+ * flags = 0 is paged_decode_attention.  The flag takes effect on the
+ * balanced split (partition_tokens = 0); fixed partitions ignore it.  Other
+ * unknown flag bits are rejected with PKV_ERR_INVALID_ARG.
+ */
+#define PKV_TABLES_READY 0x1u
+int paged_decode_attention_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *context_lens,
+                              int num_seqs, int max_blocks_per_seq, int64_t num_blocks,
+                              float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                              int block_size, int max_context_len, int partition_tokens,
+                              void *workspace, size_t workspace_bytes, float *lse_out,
+                              int32_t *err_word, void *cuda_stream, uint32_t flags);
+
+/*
  * One decode step in one call: paged_kv_append of num_tokens new tokens, then
  * paged_decode_attention, on cuda_stream.  Same arguments, results and errors
  * as the two calls in sequence (the attention's arguments are checked first,
@@ -279,6 +305,24 @@ int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
                                int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                                int max_context_len, void *workspace, size_t workspace_bytes,
                                float *lse_out, int32_t *err_word, void *cuda_stream);
+
+/*
+ * paged_decode_attention_prefix_shared with launch flags (PKV_TABLES_READY as
+ * for paged_decode_attention_ex, covering group_offsets and
+ * group_prefix_lens too).  Under the flag the shared pass reads the groups
+ * and lengths before its dependency wait and waits before it reads q or the
+ * caches; when the call runs the regular attention, that is
+ * paged_decode_attention_ex with the flag.  flags = 0 is
+ * paged_decode_attention_prefix_shared; unknown bits give PKV_ERR_INVALID_ARG.
+ */
+int paged_decode_attention_prefix_shared_ex(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads, int n_kv_heads,
+    int head_dim, int block_size, int max_context_len, const int32_t *group_offsets,
+    const int32_t *group_prefix_lens, int num_groups, int max_group_size, int max_prefix_len,
+    void *workspace, size_t workspace_bytes, float *lse_out, int32_t *err_word,
+    void *cuda_stream, uint32_t flags);
 
 /*
  * Prefix-aware decode attention over E4M3 caches: paged_decode_attention_

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     PKV_ERRBIT_CONTEXT,
     PKV_ERRBIT_SLOT,
     PKV_ERRBIT_TIMEOUT,
+    PKV_TABLES_READY,
     PagedKVError,
     decode_plan,
     decode_plan_fp8,

@@ -70,6 +70,8 @@ def library():
                                                c.c_float, c.c_int, c.c_int, c.c_int, c.c_int,
                                                c.c_int, c.c_int, p, c.c_size_t, p, p, p]
         lib.paged_decode_attention.restype = c.c_int
+        lib.paged_decode_attention_ex.argtypes = lib.paged_decode_attention.argtypes + [c.c_uint32]
+        lib.paged_decode_attention_ex.restype = c.c_int
         lib.paged_kv_get_error.argtypes = [p, p, c.POINTER(c.c_int32)]
         lib.paged_kv_get_error.restype = c.c_int
         lib.paged_kv_status_string.argtypes = [c.c_int]
@@ -146,16 +148,22 @@ def decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_block
     return P.value, W.value
 
 
+PKV_TABLES_READY = 0x1
+
+
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, n_q_heads,
                            n_kv_heads, head_dim, block_size, max_context_len=None,
                            partition_tokens=0, out=None, workspace=None, lse=None,
-                           err_word=None):
+                           err_word=None, flags=0):
     """softmax(q K^T * scale) V over each sequence's paged K/V -> out [B, H, d] fp16.
 
     q [B, H, d] fp16; k_cache/v_cache [NB, Hk, bs, d] fp16; block_tables
     [B, MB] int32; context_lens [B] int32.  max_context_len: an upper bound on
     context_lens (None -> MB * bs; pass the host-side value to keep the launch
     free of a device sync).  lse: optional fp32 [B, H] output tensor.
+    flags: 0 (paged_decode_attention) or PKV_TABLES_READY
+    (paged_decode_attention_ex: the kernel launched just before on the
+    current stream writes neither context_lens nor block_tables).
     """
     dev = q.device
     _need(q, "q", torch.float16, dev)
@@ -193,14 +201,16 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
             workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         else:
             _need(workspace, "workspace", torch.uint8, dev)
-    with torch.cuda.device(dev):
-        rc = library().paged_decode_attention(
-            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
             _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), n_q_heads, n_kv_heads,
             head_dim, block_size, mcl, P, _ptr(workspace) if ws_bytes > 0 else None,
-            workspace.numel() if (ws_bytes > 0) else 0, _ptr(lse), _ptr(err_word),
-            _stream_handle(dev))
-    _check("paged_decode_attention", rc)
+            workspace.numel() if (ws_bytes > 0) else 0, _ptr(lse), _ptr(err_word))
+    with torch.cuda.device(dev):
+        if flags:
+            rc = library().paged_decode_attention_ex(*args, _stream_handle(dev), int(flags))
+        else:
+            rc = library().paged_decode_attention(*args, _stream_handle(dev))
+    _check("paged_decode_attention_ex" if flags else "paged_decode_attention", rc)
     return out
 
 
@@ -297,10 +307,14 @@ def prefix_shared_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size
 def _prefix_shared_call(scales, q, k_cache, v_cache, block_tables, context_lens, scale,
                         n_q_heads, n_kv_heads, head_dim, block_size, group_offsets,
                         group_prefix_lens, max_group_size, max_prefix_len, max_context_len, out,
-                        workspace, lse, err_word):
-    """scales: None (fp16 caches) or (k_scale, v_scale) of E4M3 caches."""
+                        workspace, lse, err_word, flags=0):
+    """scales: None (fp16 caches) or (k_scale, v_scale) of E4M3 caches;
+    flags (fp16 only): launch flags of paged_decode_attention_prefix_shared_ex."""
     fp8 = scales is not None
-    name = "paged_decode_attention_prefix_shared" + ("_fp8" if fp8 else "")
+    if fp8 and flags:
+        raise ValueError("launch flags are taken by the fp16 call only")
+    name = "paged_decode_attention_prefix_shared" + ("_fp8" if fp8 else "") + \
+        ("_ex" if flags else "")
     lib = library()
     fn = getattr(lib, name)
     c = ctypes
@@ -308,7 +322,7 @@ def _prefix_shared_call(scales, q, k_cache, v_cache, block_tables, context_lens,
     fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float] + \
         ([c.c_float, c.c_float] if fp8 else []) + \
         [c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, p, c.c_int, c.c_int, c.c_int, p,
-         c.c_size_t, p, p, p]
+         c.c_size_t, p, p, p] + ([c.c_uint32] if flags else [])
     fn.restype = c.c_int
     dev = q.device
     kv_dtype = torch.uint8 if fp8 else torch.float16
@@ -346,7 +360,7 @@ def _prefix_shared_call(scales, q, k_cache, v_cache, block_tables, context_lens,
                 n_kv_heads, head_dim, block_size, mcl, _ptr(group_offsets),
                 _ptr(group_prefix_lens), G, int(max_group_size), int(max_prefix_len),
                 _ptr(workspace), workspace.numel(), _ptr(lse), _ptr(err_word),
-                _stream_handle(dev))
+                _stream_handle(dev), *([int(flags)] if flags else []))
     _check(name, rc)
     return out
 
@@ -355,14 +369,15 @@ def paged_decode_attention_prefix_shared(q, k_cache, v_cache, block_tables, cont
                                          n_q_heads, n_kv_heads, head_dim, block_size,
                                          group_offsets, group_prefix_lens, max_group_size,
                                          max_prefix_len, max_context_len=None, out=None,
-                                         workspace=None, lse=None, err_word=None):
+                                         workspace=None, lse=None, err_word=None, flags=0):
     """Decode attention that reads each group's shared prefix blocks once per
     chunk of members.  group_offsets [G+1] and group_prefix_lens [G] are int32
-    CUDA tensors (consecutive ranges of sequences, shared prefix tokens)."""
+    CUDA tensors (consecutive ranges of sequences, shared prefix tokens).
+    flags: 0, or PKV_TABLES_READY (paged_decode_attention_prefix_shared_ex)."""
     return _prefix_shared_call(None, q, k_cache, v_cache, block_tables, context_lens, scale,
                                n_q_heads, n_kv_heads, head_dim, block_size, group_offsets,
                                group_prefix_lens, max_group_size, max_prefix_len,
-                               max_context_len, out, workspace, lse, err_word)
+                               max_context_len, out, workspace, lse, err_word, flags)
 
 
 def paged_decode_attention_prefix_shared_fp8(q, k_cache, v_cache, block_tables, context_lens,

@@ -197,6 +197,23 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                                  workspace, workspace_bytes, lse_out, err_word, cuda_stream, 0);
 }
 
+int paged_decode_attention_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *context_lens,
+                              int num_seqs, int max_blocks_per_seq, int64_t num_blocks,
+                              float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                              int block_size, int max_context_len, int partition_tokens,
+                              void *workspace, size_t workspace_bytes, float *lse_out,
+                              int32_t *err_word, void *cuda_stream, uint32_t flags) {
+    if (flags & ~PKV_TABLES_READY) return PKV_ERR_INVALID_ARG;
+    // with the tables ready, the kernel before writes at most q, the caches
+    // and the workspace: the same contract as after this library's append
+    return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                 max_blocks_per_seq, num_blocks, scale, n_q_heads, n_kv_heads,
+                                 head_dim, block_size, max_context_len, partition_tokens,
+                                 workspace, workspace_bytes, lse_out, err_word, cuda_stream,
+                                 (flags & PKV_TABLES_READY) ? 2 : 0);
+}
+
 int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                       int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
                       const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
@@ -546,7 +563,10 @@ int prefix_shared_impl(void *out, const void *q, const void *k_cache, const void
                        int block_size, int max_context_len, const int32_t *group_offsets,
                        const int32_t *group_prefix_lens, int num_groups, int max_group_size,
                        int max_prefix_len, void *workspace, size_t workspace_bytes,
-                       float *lse_out, int32_t *err_word, void *cuda_stream) {
+                       float *lse_out, int32_t *err_word, void *cuda_stream,
+                       uint32_t flags = 0) {
+    if (flags & ~PKV_TABLES_READY) return PKV_ERR_INVALID_ARG;
+    const bool ready = (flags & PKV_TABLES_READY) != 0;
     if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if (fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
                 !(v_scale > 0.f)))
@@ -577,7 +597,7 @@ int prefix_shared_impl(void *out, const void *q, const void *k_cache, const void
                                            num_seqs, max_blocks_per_seq, num_blocks, scale,
                                            n_q_heads, n_kv_heads, head_dim, block_size,
                                            max_context_len, 0, workspace, workspace_bytes,
-                                           lse_out, err_word, cuda_stream, 0);
+                                           lse_out, err_word, cuda_stream, ready ? 2 : 0);
     if (!workspace || workspace_bytes < sp.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     if (static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
@@ -618,7 +638,9 @@ int prefix_shared_impl(void *out, const void *q, const void *k_cache, const void
     a.sh_acc = reinterpret_cast<float *>(base + sp.sh_acc);
     a.sh_m = reinterpret_cast<float *>(base + sp.sh_m);
     a.sh_l = reinterpret_cast<float *>(base + sp.sh_l);
-    a.defer_dep_wait = num_groups > 0 ? 1 : 0;  // the shared pass runs just before
+    // the suffix pass: after the shared pass (see its wait), else on its own
+    a.defer_dep_wait = num_groups > 0 ? 1 : (ready ? 2 : 0);
+    a.sh_tables_ready = ready ? 1 : 0;
     a.first_wait_polls = pkv::test_wait_polls();
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e = cudaSuccess;
@@ -645,6 +667,21 @@ int paged_decode_attention_prefix_shared(
                               n_kv_heads, head_dim, block_size, max_context_len, group_offsets,
                               group_prefix_lens, num_groups, max_group_size, max_prefix_len,
                               workspace, workspace_bytes, lse_out, err_word, cuda_stream);
+}
+
+int paged_decode_attention_prefix_shared_ex(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads, int n_kv_heads,
+    int head_dim, int block_size, int max_context_len, const int32_t *group_offsets,
+    const int32_t *group_prefix_lens, int num_groups, int max_group_size, int max_prefix_len,
+    void *workspace, size_t workspace_bytes, float *lse_out, int32_t *err_word,
+    void *cuda_stream, uint32_t flags) {
+    return prefix_shared_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              max_blocks_per_seq, num_blocks, scale, 1.f, 1.f, false, n_q_heads,
+                              n_kv_heads, head_dim, block_size, max_context_len, group_offsets,
+                              group_prefix_lens, num_groups, max_group_size, max_prefix_len,
+                              workspace, workspace_bytes, lse_out, err_word, cuda_stream, flags);
 }
 
 int paged_decode_attention_prefix_shared_fp8(

@@ -108,23 +108,36 @@ __global__ void __launch_bounds__(kWS * 32)
                             ? reinterpret_cast<const char *>(a.context_lens) + ln * 128
                             : reinterpret_cast<const char *>(a.block_tables) + (ln - len_lines) * 128);
     }
-    grid_dependency_wait();
-    // Everything before this grid in the stream is complete now, so the
-    // suffix pass that follows may be scheduled as this grid's CTAs retire:
-    // it reads nothing this grid writes before its own dependency wait, and
-    // what it reads before that wait (lengths, tables, the private K/V)
-    // was written before this grid started.
-    allow_dependent_launch();
+    // Everything before this grid in the stream is complete after the wait,
+    // so the suffix pass that follows may be scheduled as this grid's CTAs
+    // retire: it reads nothing this grid writes before its own dependency
+    // wait, and what it reads before that wait (lengths, tables, the private
+    // K/V) was written before this grid started.  With sh_tables_ready the
+    // kernel before writes no lengths, tables or groups, so the group's
+    // bounds and shortest member are read before the wait.
+    if (!a.sh_tables_ready) {
+        grid_dependency_wait();
+        allow_dependent_launch();
+    }
     const int first = a.group_offsets[gi];
     const int count = a.group_offsets[gi + 1] - first;
     const int m0 = chunk * MPC;
-    if (count < 2 || m0 >= count) return;  // CTA-uniform
+    if (count < 2 || m0 >= count) {  // CTA-uniform
+        // an exit counts as this CTA's trigger: wait first, so that the
+        // suffix pass's early reads never run ahead of the kernel before
+        if (a.sh_tables_ready) grid_dependency_wait();
+        return;
+    }
     const int nm = min(MPC, count - m0);
 
     // shared tiles of the group (the same rule as the private-suffix kernel)
     __syncthreads();
     for (int i = tid; i < count; i += nthreads) atomicMin(&s_min_len, shared_len_of(a, first + i));
     __syncthreads();
+    if (a.sh_tables_ready) {  // q and the caches may come from the kernel before
+        grid_dependency_wait();
+        allow_dependent_launch();
+    }
     const int St = shared_tiles(a, gi, s_min_len);
     const int PT = a.sh_part_tiles;
     const int t0 = part * PT;

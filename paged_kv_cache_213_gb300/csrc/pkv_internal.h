@@ -75,6 +75,8 @@ struct DecodeArgs {
     int sh_parts;                 // partitions of the shared prefix
     int sh_part_tiles;            // 16-token tiles per partition
     int sh_warps;                 // warps per shared-pass CTA
+    int sh_tables_ready = 0;      // shared pass: the kernel before writes no
+                                  // lengths, tables or groups (PKV_TABLES_READY)
     float *sh_acc;                // [B][H][sh_parts][D] shared-pass partial sums
     float *sh_m;                  // [B][H][sh_parts]
     float *sh_l;                  // [B][H][sh_parts]
@@ -84,9 +86,10 @@ struct DecodeArgs {
     //  1: the kernel before is the shared-prefix pass, which writes only
     //     sh_acc / sh_m / sh_l: prologue and private tiles run before the
     //     wait, which comes before the first read of those partials;
-    //  2: the kernel before is this library's append, which writes only the
-    //     caches: the prologue (lengths, block ids) runs before the wait,
-    //     which comes before the first K/V load.
+    //  2: the kernel before writes no lengths or tables (this library's
+    //     append, or a caller's kernel under PKV_TABLES_READY): the prologue
+    //     (lengths, block ids, split) runs before the wait, which comes
+    //     before the first read of q, the caches or the workspace.
     int defer_dep_wait;
     // FP8 caches (balanced kernel only): k_cache / v_cache hold E4M3 codes,
     // scale_log2 already includes k_scale, and outputs are multiplied by v_scale

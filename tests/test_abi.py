@@ -105,6 +105,15 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert call(fake, fake, fake, fake, fake, fake, ws=fake, ws_bytes=64) == -3
     assert call(fake, fake, fake, fake, fake, fake, scale=float("nan")) == -1
     assert lib.paged_kv_get_error(n, n, n) == -1
+    # the flagged call: the same checks, and unknown flag bits are rejected first
+
+    def call_ex(flags, out=fake, ws=None):
+        return lib.paged_decode_attention_ex(out, fake, fake, fake, fake, fake, args["B"],
+                                             args["MB"], args["NB"], 0.1, args["H"], args["Hk"],
+                                             args["d"], args["bs"], 0, 64, ws, 0, n, n, n, flags)
+    assert call_ex(0x2) == -1 and call_ex(0xffff0000) == -1
+    assert call_ex(pkv.PKV_TABLES_READY, out=n) == -1
+    assert call_ex(pkv.PKV_TABLES_READY) == -3                     # no workspace
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="a GPU is present")
@@ -223,3 +232,11 @@ def test_prefix_shared_call_rejects_bad_arguments(lib):
     assert call(offs=None) == -1                      # groups without their offsets
     assert call(pref=None) == -1
     assert call(offs=odd) == -1                       # int32 arrays must be 4-byte aligned
+    ex = lib.paged_decode_attention_prefix_shared_ex
+    ex.argtypes = fn.argtypes + [c.c_uint32]
+    ex.restype = c.c_int
+    # unknown flag bits are rejected first; the flag itself changes no host check
+    assert ex(x, x, x, x, x, x, 4, 8, 40, 0.1, 8, 2, 128, 16, 256, x, x, 2, 2, 64, x, 1 << 22,
+              None, None, None, 0x4) == -1
+    assert ex(x, x, x, x, x, x, 4, 8, 0, 0.1, 8, 2, 128, 16, 256, x, x, 2, 2, 64, x, 1 << 22,
+              None, None, None, pkv.PKV_TABLES_READY) == -1

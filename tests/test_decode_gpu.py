@@ -318,3 +318,41 @@ def test_decode_step_matches_append_then_attend(cfg):
     ref = oracle_step(batch)
     assert_close(out.cpu().numpy(), ref["out"], what=f"step {cfg}")
     assert np.max(np.abs(lse.cpu().numpy() - ref["lse"])) <= 1e-4
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_tables_ready_flag(cfg):
+    """paged_decode_attention_ex with PKV_TABLES_READY, launched right after
+    kernels that write the caches (the append) or the workspace (its zero
+    fill), then back to back with itself on one workspace: bit-identical to
+    the plain call, and the oracle's result, every output."""
+    batch = wl.workload(cfg, poison=True)
+    dev = to_dev(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, ws = pkv.decode_plan(batch.num_seqs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
+                            batch.block_size, batch.max_blocks_per_seq, batch.max_context_len, 0)
+    work = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    work.zero_()  # the kernel just before the first call writes the workspace
+    if batch.has_append:  # ... or the caches
+        pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                            dev["v_cache"], err_word=err)
+
+    def call(flags):
+        lse = torch.full((batch.num_seqs, batch.n_q_heads), float("nan"), device="cuda")
+        out = pkv.paged_decode_attention(
+            dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+            batch.scale, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size,
+            max_context_len=batch.max_context_len, workspace=work, lse=lse, err_word=err,
+            flags=flags)
+        return out, lse
+    first = call(pkv.PKV_TABLES_READY)
+    second = call(pkv.PKV_TABLES_READY)
+    plain = call(0)
+    assert pkv.get_error(err) == 0
+    o1, l1 = (t.cpu().numpy() for t in first)
+    for o, l in (second, plain):
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), o1.view(np.uint16))
+        assert np.array_equal(l.cpu().numpy(), l1)
+    ref = oracle_step(batch)
+    assert_close(o1, ref["out"], what=f"flagged workload {cfg}")
+    assert np.max(np.abs(l1.astype(np.float64) - ref["lse"])) <= 1e-4

@@ -23,22 +23,22 @@ def _cuda():
     pkv.library()
 
 
-def run_shared(batch, groups=None, pass_="shared"):
+def run_shared(batch, groups=None, pass_="shared", flags=0):
     """The prefix-aware entry point; pass_ fixes its choice between the
     two-pass path ("shared") and the regular attention ("regular"), or leaves
-    it to the library (None)."""
+    it to the library (None); flags are its launch flags."""
     saved = os.environ.pop("PKV_PREFIX_PASS", None)
     if pass_ is not None:
         os.environ["PKV_PREFIX_PASS"] = pass_
     try:
-        return _run_shared(batch, groups)
+        return _run_shared(batch, groups, flags)
     finally:
         os.environ.pop("PKV_PREFIX_PASS", None)
         if saved is not None:
             os.environ["PKV_PREFIX_PASS"] = saved
 
 
-def _run_shared(batch, groups=None):
+def _run_shared(batch, groups=None, flags=0):
     offs, pref, gmax, pmax = groups if groups is not None else wl.prefix_groups(batch)
     dev = to_dev(batch)
     if batch.has_append:
@@ -50,7 +50,7 @@ def _run_shared(batch, groups=None):
         dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
         batch.scale, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size,
         torch.from_numpy(offs).cuda(), torch.from_numpy(pref).cuda(), gmax, pmax,
-        max_context_len=batch.max_context_len, lse=lse, err_word=err)
+        max_context_len=batch.max_context_len, lse=lse, err_word=err, flags=flags)
     assert pkv.get_error(err) == 0
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy().astype(np.float64)
@@ -126,3 +126,19 @@ def test_many_groups_of_forked_completions():
         out, lse = run_shared(batch, pass_=pass_)
         assert_close(out, ref["out"], what=f"pass={pass_}")
         assert np.max(np.abs(lse - ref["lse"])) <= 1e-4
+
+
+@pytest.mark.parametrize("pass_", ["shared", "regular"])
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_tables_ready_flag(cfg, pass_):
+    """paged_decode_attention_prefix_shared_ex with PKV_TABLES_READY (the
+    groups and lengths read before the dependency wait): bit-identical to the
+    call without the flag, every output against the oracle."""
+    batch = wl.workload(cfg, poison=True)
+    out_f, lse_f = run_shared(batch, pass_=pass_, flags=pkv.PKV_TABLES_READY)
+    out_p, lse_p = run_shared(batch, pass_=pass_)
+    assert np.array_equal(out_f.view(np.uint16), out_p.view(np.uint16))
+    assert np.array_equal(lse_f, lse_p)
+    ref = oracle_step(batch)
+    assert_close(out_f, ref["out"], what=f"flagged workload {cfg}")
+    assert np.max(np.abs(lse_f - ref["lse"])) <= 1e-4
