@@ -607,6 +607,7 @@ __global__ void __launch_bounds__(kW * 32)
         // position v0 - kCut - 1) lies before warp wf's positions
         const bool wf_starts_here = x0 == 0 || static_cast<long long>(wf) * U > v0 - kCut - 1;
         constexpr int cap = static_cast<int>(C::REGION_BYTES / REC);
+        static_assert(cap >= 1, "a warp's region must hold a merge record");
         float M = -INFINITY, Lsum = 0.f, Mh = -INFINITY, Lh = 0.f;
 #pragma unroll
         for (int nb = 0; nb < C::NB_D; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;

@@ -84,6 +84,9 @@ struct PipeCfg : MmaCfg<D> {
     static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 1023) / 1024 * 1024;
     // cross-CTA record of one head: acc [G][D], m [G], l [G], padded to 16 bytes
     static constexpr size_t REC = (static_cast<size_t>(G) * (D + 2) * 4 + 15) / 16 * 16;
+    // a consumer's slice of a ring of at least two stages holds a record, so
+    // that a merge round always stages one or more
+    static_assert(2 * STAGE_BYTES / HK >= static_cast<int>(REC) + 16, "merge slice");
 };
 
 struct __align__(16) UnitMeta {
