@@ -356,3 +356,40 @@ def test_tables_ready_flag(cfg):
     ref = oracle_step(batch)
     assert_close(o1, ref["out"], what=f"flagged workload {cfg}")
     assert np.max(np.abs(l1.astype(np.float64) - ref["lse"])) <= 1e-4
+
+
+@pytest.mark.parametrize("what", ["tables", "lengths", "both"])
+def test_plain_call_after_a_kernel_that_rewrites_the_tables(what):
+    """A plain call plans its split before its dependency wait and checks the
+    lengths and block ids it read once the wait is over; when the kernel just
+    before it rewrites them (here an elementwise kernel storing the real
+    values over stale ones), the call must attend over the new ones."""
+    batch = wl.workload(2, poison=True)
+    dev = to_dev(batch)
+    pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                        dev["v_cache"])
+    good_bt, good_cl = dev["block_tables"].clone(), dev["context_lens"].clone()
+    stale_bt = good_bt.flip(0).contiguous()  # other sequences' (valid) block ids
+    stale_cl = (good_cl // 2 + 1).contiguous()
+    ref = oracle_step(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, ws = pkv.decode_plan(batch.num_seqs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
+                            batch.block_size, batch.max_blocks_per_seq, batch.max_context_len, 0)
+    work = torch.zeros(ws, dtype=torch.uint8, device="cuda")
+    for _ in range(4):
+        if what in ("tables", "both"):
+            dev["block_tables"].copy_(stale_bt)
+        if what in ("lengths", "both"):
+            dev["context_lens"].copy_(stale_cl)
+        torch.cuda.synchronize()
+        # the kernels just before the call write the real values
+        if what in ("tables", "both"):
+            torch.add(good_bt, 0, out=dev["block_tables"])
+        if what in ("lengths", "both"):
+            torch.add(good_cl, 0, out=dev["context_lens"])
+        out = pkv.paged_decode_attention(
+            dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+            batch.scale, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size,
+            max_context_len=batch.max_context_len, workspace=work, err_word=err)
+        assert pkv.get_error(err) == 0
+        assert_close(out.cpu().numpy(), ref["out"], what=f"after rewritten {what}")
