@@ -364,8 +364,8 @@ class Path:
             self.ws_bytes = plan(B, H, Hk, D, bs, MB, mcl, len(pref), gmax, pmax)
             self.attn_launches = 2
         self.step_launches = self.attn_launches + (1 if self.has_append else 0)
-        # launch flags of the plain fp16 attention call (PKV_TABLES_READY where
-        # the caller knows that the kernel before writes no lengths or tables)
+        # launch flags of the attention call (PKV_TABLES_READY where the caller
+        # knows that the kernel before writes no lengths or tables)
         self.attn_flags = 0
         self.copies = [first] + [{k: v.clone() for k, v in first.items()}
                                  for _ in range(copies - 1)]
@@ -384,18 +384,19 @@ class Path:
             pkv.paged_decode_attention_multi(c["q"], c["kc"], c["vc"], c["bt"], c["cl"],
                                              c["qstart"], bt.scale, H, Hk, D, bs, self.nq,
                                              max_context_len=mcl, partition_tokens=self.P,
-                                             out=c["out"], workspace=ws, err_word=c["err"])
+                                             out=c["out"], workspace=ws, err_word=c["err"],
+                                             flags=self.attn_flags)
         elif self.fp8 and self.groups is not None:
             gmax, pmax, _ = self.groups
             pkv.paged_decode_attention_prefix_shared_fp8(
                 c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale, self.k_scale, self.v_scale,
                 H, Hk, D, bs, c["offs"], c["pref"], gmax, pmax, max_context_len=mcl,
-                out=c["out"], workspace=ws, err_word=c["err"])
+                out=c["out"], workspace=ws, err_word=c["err"], flags=self.attn_flags)
         elif self.fp8:
             pkv.paged_decode_attention_fp8(c["q"], c["kc"], c["vc"], c["bt"], c["cl"], bt.scale,
                                            self.k_scale, self.v_scale, H, Hk, D, bs,
                                            max_context_len=mcl, out=c["out"], workspace=ws,
-                                           err_word=c["err"])
+                                           err_word=c["err"], flags=self.attn_flags)
         elif self.groups is not None:
             gmax, pmax, _ = self.groups
             pkv.paged_decode_attention_prefix_shared(
@@ -409,9 +410,9 @@ class Path:
                                        flags=self.attn_flags)
 
     def flaggable(self):
-        """The attention call is a plain or prefix-aware fp16 one, which take
-        launch flags."""
-        return not (self.multi or self.fp8)
+        """The attention call takes launch flags (every entry point here has
+        an _ex form)."""
+        return True
 
     def step(self, i):
         """append + attention: one library call when the step has an append on
@@ -568,16 +569,17 @@ def kernel_label(path, torch, device):
     library's dispatch rule, restated for the label only)."""
     bt = path.batch
     if path.multi:
-        return ("paged_decode_attention_multi: decode_balanced_kernel with multi-token rows "
-                "(one launch)" if path.P == 0 else
+        return ("paged_decode_attention_multi_ex (PKV_TABLES_READY): decode_balanced_kernel "
+                "with multi-token rows (one launch)" if path.P == 0 else
                 "paged_decode_attention_multi: decode_multi_kernel + multi_merge_kernel")
     if path.groups is not None:
-        return ("paged_decode_attention_prefix_shared" +
-                ("_fp8" if path.fp8 else "_ex (PKV_TABLES_READY)") +
-                ": decode_shared_kernel (shared pass) + decode_balanced_kernel (suffix pass), "
-                "or the regular call when the shared blocks fit in L2")
+        return ("paged_decode_attention_prefix_shared" + ("_fp8" if path.fp8 else "") +
+                "_ex (PKV_TABLES_READY): decode_shared_kernel (shared pass) + "
+                "decode_balanced_kernel (suffix pass), or the regular call when the shared "
+                "blocks fit in L2")
     if path.fp8:
-        return "paged_decode_attention_fp8: decode_balanced_kernel on E4M3 tiles (one launch)"
+        return ("paged_decode_attention_fp8_ex (PKV_TABLES_READY): decode_balanced_kernel on "
+                "E4M3 tiles (one launch)")
     if path.P != 0:
         return "paged_decode_attention: partition kernel + LSE merge kernel"
     sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -620,9 +622,8 @@ def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CO
         if any(path.errors()):
             raise SystemExit(f"bench.py: device error word on row {key}")
         ms, ms_iso = statistics.fmean(b2b), statistics.fmean(iso)
-        entry = ("paged_decode_attention_multi" if nq > 1 else
-                 "paged_decode_attention" + ("_prefix_shared" if prefix else "") +
-                 ("_fp8" if fp8 else "") +
+        entry = ("paged_decode_attention" + ("_multi" if nq > 1 else "") +
+                 ("_prefix_shared" if prefix else "") + ("_fp8" if fp8 else "") +
                  ("_ex (PKV_TABLES_READY)" if plain is not None else ""))
         rows[key] = {
             "workload": wl.WORKLOADS[w], "entry": entry,
@@ -730,8 +731,8 @@ def run_ours(args):
     # the dominant call alone, both ways.  Back to back, each call is made as
     # in a decode loop whose tables are copied in before the layers run: the
     # kernel before it (the previous call) writes no lengths or tables, so the
-    # plain fp16 call takes PKV_TABLES_READY; the same calls without the flag
-    # are timed too (attention_ms_plain_call).
+    # call takes PKV_TABLES_READY; the same calls without the flag are timed
+    # too (attention_ms_plain_call).
     attn_plain = None
     if path.flaggable():
         attn_plain = timer.back_to_back(lambda i: path.attend(i % ROTATE), args.steps)
@@ -834,7 +835,7 @@ def run_ours(args):
                                               4) if attn_plain is not None else None,
                      "kernel": kernel_label(path, torch, device),
                      "timing": "achieved = attention bytes / attention_ms (back-to-back "
-                               "calls, PKV_TABLES_READY on the plain fp16 call); "
+                               "calls, made with PKV_TABLES_READY); "
                                "frac_plain_call: the same calls without the flag; "
                                "frac_isolated uses attention_ms_isolated",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"

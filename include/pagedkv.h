@@ -325,6 +325,19 @@ int paged_decode_attention_prefix_shared_ex(
     void *cuda_stream, uint32_t flags);
 
 /*
+ * paged_decode_attention_fp8 with launch flags (PKV_TABLES_READY, as for
+ * paged_decode_attention_ex).  flags = 0 is paged_decode_attention_fp8.
+ */
+int paged_decode_attention_fp8_ex(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                  float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
+                                  int head_dim, int block_size, int max_context_len,
+                                  void *workspace, size_t workspace_bytes, float *lse_out,
+                                  int32_t *err_word, void *cuda_stream, uint32_t flags);
+
+/*
  * Prefix-aware decode attention over E4M3 caches: paged_decode_attention_
  * prefix_shared with the caches, scales and results of
  * paged_decode_attention_fp8 (same reading of the FP8 format and scales; the
@@ -350,6 +363,15 @@ int paged_decode_attention_prefix_shared_fp8(
     const int32_t *group_offsets, const int32_t *group_prefix_lens, int num_groups,
     int max_group_size, int max_prefix_len, void *workspace, size_t workspace_bytes,
     float *lse_out, int32_t *err_word, void *cuda_stream);
+/* The same with launch flags (PKV_TABLES_READY, covering the groups too). */
+int paged_decode_attention_prefix_shared_fp8_ex(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, float k_scale, float v_scale,
+    int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
+    const int32_t *group_offsets, const int32_t *group_prefix_lens, int num_groups,
+    int max_group_size, int max_prefix_len, void *workspace, size_t workspace_bytes,
+    float *lse_out, int32_t *err_word, void *cuda_stream, uint32_t flags);
 
 /*
  * Multi-token (causal) paged attention: several new tokens of each sequence
@@ -398,6 +420,21 @@ int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
                                  int max_context_len, int partition_tokens, void *workspace,
                                  size_t workspace_bytes, float *lse_out, int32_t *err_word,
                                  void *cuda_stream);
+/*
+ * paged_decode_attention_multi with launch flags: PKV_TABLES_READY as for
+ * paged_decode_attention_ex, covering query_start too.  It takes effect on
+ * the balanced split; fixed partitions ignore it.  flags = 0 is
+ * paged_decode_attention_multi; unknown bits give PKV_ERR_INVALID_ARG.
+ */
+int paged_decode_attention_multi_ex(void *out, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_tables,
+                                    const int32_t *context_lens, const int32_t *query_start,
+                                    int num_seqs, int total_q, int max_q_len,
+                                    int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                    int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                    int max_context_len, int partition_tokens, void *workspace,
+                                    size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                                    void *cuda_stream, uint32_t flags);
 
 /*
  * Allocation-free variant of paged_decode_attention.  The pages have no

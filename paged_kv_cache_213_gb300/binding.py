@@ -309,10 +309,8 @@ def _prefix_shared_call(scales, q, k_cache, v_cache, block_tables, context_lens,
                         group_prefix_lens, max_group_size, max_prefix_len, max_context_len, out,
                         workspace, lse, err_word, flags=0):
     """scales: None (fp16 caches) or (k_scale, v_scale) of E4M3 caches;
-    flags (fp16 only): launch flags of paged_decode_attention_prefix_shared_ex."""
+    flags: launch flags (the _ex entry points)."""
     fp8 = scales is not None
-    if fp8 and flags:
-        raise ValueError("launch flags are taken by the fp16 call only")
     name = "paged_decode_attention_prefix_shared" + ("_fp8" if fp8 else "") + \
         ("_ex" if flags else "")
     lib = library()
@@ -385,13 +383,13 @@ def paged_decode_attention_prefix_shared_fp8(q, k_cache, v_cache, block_tables, 
                                              head_dim, block_size, group_offsets,
                                              group_prefix_lens, max_group_size, max_prefix_len,
                                              max_context_len=None, out=None, workspace=None,
-                                             lse=None, err_word=None):
+                                             lse=None, err_word=None, flags=0):
     """The prefix-aware call over E4M3 caches (uint8 codes; values code *
-    k_scale and code * v_scale)."""
+    k_scale and code * v_scale).  flags: 0, or PKV_TABLES_READY."""
     return _prefix_shared_call((k_scale, v_scale), q, k_cache, v_cache, block_tables,
                                context_lens, scale, n_q_heads, n_kv_heads, head_dim, block_size,
                                group_offsets, group_prefix_lens, max_group_size, max_prefix_len,
-                               max_context_len, out, workspace, lse, err_word)
+                               max_context_len, out, workspace, lse, err_word, flags)
 
 
 # ---------------------------------------------------------------------------
@@ -450,16 +448,18 @@ def decode_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_b
 def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
                                v_scale, n_q_heads, n_kv_heads, head_dim, block_size,
                                max_context_len=None, out=None, workspace=None, lse=None,
-                               err_word=None):
+                               err_word=None, flags=0):
     """Decode attention over E4M3 caches [NB, Hk, bs, d] (uint8): keys and values are
-    code * k_scale and code * v_scale.  Returns out [B, H, d] fp16."""
+    code * k_scale and code * v_scale.  Returns out [B, H, d] fp16.  flags: 0, or
+    PKV_TABLES_READY (paged_decode_attention_fp8_ex)."""
     lib = library()
-    fn = lib.paged_decode_attention_fp8
+    name = "paged_decode_attention_fp8" + ("_ex" if flags else "")
+    fn = getattr(lib, name)
     c = ctypes
     p = c.c_void_p
     fn.argtypes = [p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float, c.c_float,
                    c.c_float, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p,
-                   p]
+                   p] + ([c.c_uint32] if flags else [])
     fn.restype = c.c_int
     dev = q.device
     _need(q, "q", torch.float16, dev)
@@ -495,8 +495,8 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, 
                 _ptr(context_lens), B, MB, k_cache.shape[0], float(scale), float(k_scale),
                 float(v_scale), n_q_heads, n_kv_heads, head_dim, block_size, mcl,
                 _ptr(workspace), workspace.numel(), _ptr(lse), _ptr(err_word),
-                _stream_handle(dev))
-    _check("paged_decode_attention_fp8", rc)
+                _stream_handle(dev), *([int(flags)] if flags else []))
+    _check(name, rc)
     return out
 
 
@@ -523,18 +523,21 @@ def multi_plan(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim, bl
 def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, query_start,
                                  scale, n_q_heads, n_kv_heads, head_dim, block_size, max_q_len,
                                  max_context_len=None, partition_tokens=0, out=None,
-                                 workspace=None, lse=None, err_word=None):
+                                 workspace=None, lse=None, err_word=None, flags=0):
     """Causal attention of each sequence's last n_b tokens over its paged K/V.
 
     q [total_q, H, d] fp16 (sequence b owns rows [query_start[b], query_start[b+1]));
     query_start [B + 1] int32; context_lens include the new tokens.  Returns
-    out [total_q, H, d] fp16."""
+    out [total_q, H, d] fp16.  flags: 0, or PKV_TABLES_READY
+    (paged_decode_attention_multi_ex; the promise covers query_start)."""
     lib = library()
-    fn = lib.paged_decode_attention_multi
+    name = "paged_decode_attention_multi" + ("_ex" if flags else "")
+    fn = getattr(lib, name)
     c = ctypes
     p = c.c_void_p
     fn.argtypes = [p, p, p, p, p, p, p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_float,
-                   c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p, p]
+                   c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p,
+                   p] + ([c.c_uint32] if flags else [])
     fn.restype = c.c_int
     dev = q.device
     for t, name, dt in ((q, "q", torch.float16), (k_cache, "k_cache", torch.float16),
@@ -570,8 +573,8 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
                 _ptr(context_lens), _ptr(query_start), B, TQ, int(max_q_len), MB,
                 k_cache.shape[0], float(scale), n_q_heads, n_kv_heads, head_dim, block_size, mcl,
                 P, _ptr(workspace) if ws > 0 else None, workspace.numel() if ws > 0 else 0,
-                _ptr(lse), _ptr(err_word), _stream_handle(dev))
-    _check("paged_decode_attention_multi", rc)
+                _ptr(lse), _ptr(err_word), _stream_handle(dev), *([int(flags)] if flags else []))
+    _check(name, rc)
     return out
 
 

@@ -370,13 +370,15 @@ int paged_decode_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_
     return rc;
 }
 
-int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
-                               const void *v_cache, const int32_t *block_tables,
-                               const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
-                               int64_t num_blocks, float scale, float k_scale, float v_scale,
-                               int n_q_heads, int n_kv_heads, int head_dim, int block_size,
-                               int max_context_len, void *workspace, size_t workspace_bytes,
-                               float *lse_out, int32_t *err_word, void *cuda_stream) {
+int paged_decode_attention_fp8_ex(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                  float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
+                                  int head_dim, int block_size, int max_context_len,
+                                  void *workspace, size_t workspace_bytes, float *lse_out,
+                                  int32_t *err_word, void *cuda_stream, uint32_t flags) {
+    if (flags & ~PKV_TABLES_READY) return PKV_ERR_INVALID_ARG;
     if (num_blocks <= 0 || !std::isfinite(scale) || !std::isfinite(k_scale) ||
         !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
         return PKV_ERR_INVALID_ARG;
@@ -419,10 +421,26 @@ int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
     a.max_parts = 1;
     a.kv_fp8 = 1;
     a.v_scale = v_scale;
+    a.defer_dep_wait = (flags & PKV_TABLES_READY) ? 2 : 0;
+    a.first_wait_polls = pkv::test_wait_polls();
     const cudaError_t e =
         pkv::launch_decode_balanced(a, plan.bal, static_cast<cudaStream_t>(cuda_stream));
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                               int64_t num_blocks, float scale, float k_scale, float v_scale,
+                               int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                               int max_context_len, void *workspace, size_t workspace_bytes,
+                               float *lse_out, int32_t *err_word, void *cuda_stream) {
+    return paged_decode_attention_fp8_ex(out, q, k_cache, v_cache, block_tables, context_lens,
+                                         num_seqs, max_blocks_per_seq, num_blocks, scale, k_scale,
+                                         v_scale, n_q_heads, n_kv_heads, head_dim, block_size,
+                                         max_context_len, workspace, workspace_bytes, lse_out,
+                                         err_word, cuda_stream, 0);
 }
 
 }  // extern "C"
@@ -587,12 +605,12 @@ int prefix_shared_impl(void *out, const void *q, const void *k_cache, const void
         (lse_out && !aligned(lse_out, 4)) || (err_word && !aligned(err_word, 4)))
         return PKV_ERR_INVALID_ARG;
     if (sp.regular_path)
-        return fp8 ? paged_decode_attention_fp8(out, q, k_cache, v_cache, block_tables,
-                                                context_lens, num_seqs, max_blocks_per_seq,
-                                                num_blocks, scale, k_scale, v_scale, n_q_heads,
-                                                n_kv_heads, head_dim, block_size,
-                                                max_context_len, workspace, workspace_bytes,
-                                                lse_out, err_word, cuda_stream)
+        return fp8 ? paged_decode_attention_fp8_ex(out, q, k_cache, v_cache, block_tables,
+                                                   context_lens, num_seqs, max_blocks_per_seq,
+                                                   num_blocks, scale, k_scale, v_scale, n_q_heads,
+                                                   n_kv_heads, head_dim, block_size,
+                                                   max_context_len, workspace, workspace_bytes,
+                                                   lse_out, err_word, cuda_stream, flags)
                    : decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens,
                                            num_seqs, max_blocks_per_seq, num_blocks, scale,
                                            n_q_heads, n_kv_heads, head_dim, block_size,
@@ -700,6 +718,22 @@ int paged_decode_attention_prefix_shared_fp8(
                               cuda_stream);
 }
 
+int paged_decode_attention_prefix_shared_fp8_ex(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int64_t num_blocks, float scale, float k_scale, float v_scale,
+    int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
+    const int32_t *group_offsets, const int32_t *group_prefix_lens, int num_groups,
+    int max_group_size, int max_prefix_len, void *workspace, size_t workspace_bytes,
+    float *lse_out, int32_t *err_word, void *cuda_stream, uint32_t flags) {
+    return prefix_shared_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              max_blocks_per_seq, num_blocks, scale, k_scale, v_scale, true,
+                              n_q_heads, n_kv_heads, head_dim, block_size, max_context_len,
+                              group_offsets, group_prefix_lens, num_groups, max_group_size,
+                              max_prefix_len, workspace, workspace_bytes, lse_out, err_word,
+                              cuda_stream, flags);
+}
+
 }  // extern "C"
 
 namespace {
@@ -791,15 +825,16 @@ int paged_decode_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_he
     return PKV_OK;
 }
 
-int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
-                                 const void *v_cache, const int32_t *block_tables,
-                                 const int32_t *context_lens, const int32_t *query_start,
-                                 int num_seqs, int total_q, int max_q_len,
-                                 int max_blocks_per_seq, int64_t num_blocks, float scale,
-                                 int n_q_heads, int n_kv_heads, int head_dim, int block_size,
-                                 int max_context_len, int partition_tokens, void *workspace,
-                                 size_t workspace_bytes, float *lse_out, int32_t *err_word,
-                                 void *cuda_stream) {
+int paged_decode_attention_multi_ex(void *out, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_tables,
+                                    const int32_t *context_lens, const int32_t *query_start,
+                                    int num_seqs, int total_q, int max_q_len,
+                                    int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                    int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                    int max_context_len, int partition_tokens, void *workspace,
+                                    size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                                    void *cuda_stream, uint32_t flags) {
+    if (flags & ~PKV_TABLES_READY) return PKV_ERR_INVALID_ARG;
     if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     MultiPlan mp{};
     int rc = make_multi_plan(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim,
@@ -852,11 +887,30 @@ int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
     a.total_q = total_q;
     a.max_q_len = max_q_len;
     a.first_wait_polls = pkv::test_wait_polls();
+    // the flag covers query_start too; fixed partitions wait first thing
+    a.defer_dep_wait = (mp.balanced && (flags & PKV_TABLES_READY)) ? 2 : 0;
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = mp.balanced ? pkv::launch_decode_balanced_multi(a, mp.bal, stream)
                                       : pkv::launch_decode_multi(a, mp.row_blocks, stream);
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, const int32_t *query_start,
+                                 int num_seqs, int total_q, int max_q_len,
+                                 int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                 int max_context_len, int partition_tokens, void *workspace,
+                                 size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                                 void *cuda_stream) {
+    return paged_decode_attention_multi_ex(out, q, k_cache, v_cache, block_tables, context_lens,
+                                           query_start, num_seqs, total_q, max_q_len,
+                                           max_blocks_per_seq, num_blocks, scale, n_q_heads,
+                                           n_kv_heads, head_dim, block_size, max_context_len,
+                                           partition_tokens, workspace, workspace_bytes, lse_out,
+                                           err_word, cuda_stream, 0);
 }
 
 int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits_out) {

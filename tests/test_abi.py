@@ -114,6 +114,21 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert call_ex(0x2) == -1 and call_ex(0xffff0000) == -1
     assert call_ex(pkv.PKV_TABLES_READY, out=n) == -1
     assert call_ex(pkv.PKV_TABLES_READY) == -3                     # no workspace
+    # every _ex entry point rejects unknown flag bits before anything else
+    c = ctypes
+    p_ = c.c_void_p
+    f8 = lib.paged_decode_attention_fp8_ex
+    f8.argtypes = [p_] * 6 + [c.c_int, c.c_int, c.c_int64, c.c_float, c.c_float, c.c_float] + \
+        [c.c_int] * 5 + [p_, c.c_size_t, p_, p_, p_, c.c_uint32]
+    f8.restype = c.c_int
+    assert f8(fake, fake, fake, fake, fake, fake, 4, 8, 40, 0.1, 1.0, 1.0, 8, 2, 128, 16, 0,
+              fake, 1 << 20, n, n, n, 0x10) == -1
+    mu = lib.paged_decode_attention_multi_ex
+    mu.argtypes = [p_] * 7 + [c.c_int] * 4 + [c.c_int64, c.c_float] + [c.c_int] * 6 + \
+        [p_, c.c_size_t, p_, p_, p_, c.c_uint32]
+    mu.restype = c.c_int
+    assert mu(fake, fake, fake, fake, fake, fake, fake, 4, 8, 2, 8, 40, 0.1, 8, 2, 128, 16, 0,
+              0, fake, 1 << 20, n, n, n, 0x10) == -1
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="a GPU is present")

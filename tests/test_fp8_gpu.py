@@ -250,3 +250,37 @@ def test_fp8_prefix_shared_edge_cases(d, g):
     # the regular E4M3 call on the same caches agrees
     reg = gpu_f8(batch, kc8, vc8, ks, vs)
     assert np.max(np.abs(out.astype(np.float64) - reg["out"].astype(np.float64))) <= 2e-3
+
+
+@pytest.mark.parametrize("cfg", [2, 5])
+def test_fp8_tables_ready_flag(cfg):
+    """paged_decode_attention_fp8_ex and the prefix-aware E4M3 call with
+    PKV_TABLES_READY, back to back: bit-identical to the calls without it."""
+    batch = wl.workload(cfg, poison=True)
+    ks, vs = _scales(batch)
+    kc8, vc8 = _caches8(batch, ks, vs)
+    kc, vc = _t(kc8), _t(vc8)
+    q, bt, cl = _t(batch.q), _t(batch.block_tables), _t(batch.context_lens)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if batch.has_append:  # the kernel just before the first call writes the caches
+        pkv.paged_kv_append_fp8(_t(batch.k_new), _t(batch.v_new), _t(batch.slot_mapping), kc, vc,
+                                ks, vs, err_word=err)
+    outs = []
+    for flags in (pkv.PKV_TABLES_READY, pkv.PKV_TABLES_READY, 0):
+        outs.append(pkv.paged_decode_attention_fp8(
+            q, kc, vc, bt, cl, batch.scale, ks, vs, batch.n_q_heads, batch.n_kv_heads,
+            batch.head_dim, batch.block_size, max_context_len=batch.max_context_len,
+            err_word=err, flags=flags).cpu().numpy())
+    if batch.meta.get("shared"):
+        offs, pref, gmax, pmax = wl.prefix_groups(batch)
+        for flags in (pkv.PKV_TABLES_READY, 0):
+            outs.append(pkv.paged_decode_attention_prefix_shared_fp8(
+                q, kc, vc, bt, cl, batch.scale, ks, vs, batch.n_q_heads, batch.n_kv_heads,
+                batch.head_dim, batch.block_size, _t(offs), _t(pref), gmax, pmax,
+                max_context_len=batch.max_context_len, err_word=err, flags=flags).cpu().numpy())
+        assert np.array_equal(outs[3].view(np.uint16), outs[4].view(np.uint16))
+    assert pkv.get_error(err) == 0
+    for o in outs[1:3]:
+        assert np.array_equal(o.view(np.uint16), outs[0].view(np.uint16))
+    ref = oracle_f8(batch, kc8, vc8, ks, vs)
+    assert_close(outs[0], ref["out"], what=f"flagged fp8 workload {cfg}")

@@ -233,3 +233,24 @@ def test_balanced_split_timeout_recovers(monkeypatch):
     assert bits == 0
     ref, _ = _oracle(batch, q, qs)
     assert_close(out, ref, what="after the timeout")
+
+
+def test_tables_ready_flag():
+    """paged_decode_attention_multi_ex with PKV_TABLES_READY (lengths, tables
+    and query_start read before the dependency wait), back to back:
+    bit-identical to the call without it, and the oracle's result."""
+    rng = np.random.default_rng(83)
+    lens = rng.integers(64, 2049, 32)
+    batch, q, qs = _problem(lens, [4] * 32, 32, 8, 128, 16, 84)
+    dq, kc, vc, bt, cl, dqs = (_t(q), _t(batch.k_cache), _t(batch.v_cache),
+                               _t(batch.block_tables), _t(batch.context_lens), _t(qs))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [pkv.paged_decode_attention_multi(
+        dq, kc, vc, bt, cl, dqs, batch.scale, 32, 8, 128, 16, 4,
+        max_context_len=batch.max_context_len, err_word=err, flags=f).cpu().numpy()
+        for f in (pkv.PKV_TABLES_READY, pkv.PKV_TABLES_READY, 0)]
+    assert pkv.get_error(err) == 0
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint16), outs[0].view(np.uint16))
+    ref, _ = _oracle(batch, q, qs)
+    assert_close(outs[0], ref, what="flagged multi-token")
