@@ -84,9 +84,11 @@ constexpr int kMinUnitsSuffix = 2;
 // With eight warps per CTA (long segments, most of them cut), the split
 // counts every segment start as this many extra units.  A warp whose range
 // holds a segment's first tile is the one that releases the cut piece before
-// it, mid-loop (a GPU-scope release while its loads are in flight, about two
-// tiles' time), so it gets about that much less to stream.
-constexpr int kCutUnits = 2;
+// it, mid-loop (a GPU-scope release while its loads are in flight), and it
+// loads the segment's Q rows, so it gets less to stream.  Measured on GB300
+// (back to back, LLaMA-3-8B-shaped layer / 32k contexts): 1 unit 32.1 /
+// 162.7 us, 2 units 31.6 / 161.4, 3 units 31.5 / 162.3, 4 units 31.4 / 160.0.
+constexpr int kCutUnits = 4;
 constexpr float kLn2b = 0.69314718055994531f;
 
 template <int D, int G, bool F8, int kW, bool MT>

@@ -68,7 +68,7 @@ def check(tiles, Hk, workers, k_cut):
     return U, starts
 
 
-@pytest.mark.parametrize("k_cut", [0, 2, 3])
+@pytest.mark.parametrize("k_cut", [0, 2, 3, 4])
 def test_split_invariants_on_random_batches(k_cut):
     rng = random.Random(100 + k_cut)
     for _ in range(1000):
