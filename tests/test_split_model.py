@@ -1,7 +1,7 @@
 """The balanced kernel's work split, restated on the host and checked for
 the invariants its piece bookkeeping relies on.
 
-The kernel (decode_balanced.cu: real_at, vpos0, flush, merge) splits the
+The kernel (balanced_kernel.cuh: real_at, vpos0, flush, merge) splits the
 (KV head j, sequence b, tile t) units evenly over "virtual" units in which
 every segment (b, j) with tiles is preceded by kCut extra units: unit x of
 segment number s (in j, b order) sits at position x + kCut * (s + 1), and
