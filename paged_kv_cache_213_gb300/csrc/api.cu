@@ -769,7 +769,8 @@ int make_multi_plan(int num_seqs, int total_q, int max_q_len, int n_q_heads, int
         pkv::balanced_multi_supported(num_seqs, max_q_len, head_dim, group, block_size)) {
         // every segment's query rows fit one MMA tile: the work split evenly
         // over warps, as for decode (LLaMA-3-8B-shaped layer, 4 tokens per
-        // sequence on GB300: fixed partitions 51.4 us)
+        // sequence on GB300, calls back to back: 47.0 us on fixed partitions,
+        // 39.2 us here)
         if (!pkv::balanced_multi_plan(num_seqs, n_q_heads, n_kv_heads, head_dim,
                                       static_cast<int>(max_len), &mp->bal))
             return PKV_ERR_CUDA;
