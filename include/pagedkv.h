@@ -50,7 +50,8 @@
  * pkv_status and launches nothing.  Problems only the device can see (a
  * block id outside [0, num_blocks), a slot beyond the pool, a context length
  * outside [0, max_blocks_per_seq * block_size] or above max_context_len, a
- * copy that did not complete within about a second) set bits in the optional
+ * copy that did not complete within about a second, a workspace whose
+ * arrival counters did not start at zero) set bits in the optional
  * device word *err_word (PKV_ERRBIT_*): the offending block or token is
  * skipped, nothing traps, and the result for that sequence is unspecified.
  * Read the word with paged_kv_get_error.  Launch failures return
@@ -81,6 +82,27 @@ typedef enum pkv_status {
 #define PKV_ERRBIT_CONTEXT 0x4  /* context length < 0, > max_blocks_per_seq*block_size,
                                    or > max_context_len */
 #define PKV_ERRBIT_TIMEOUT 0x8  /* a bounded wait for a block copy gave up */
+#define PKV_ERRBIT_WORKSPACE 0x10 /* an arrival counter of the workspace did not
+                                     start at zero (see PKV_WORKSPACE_COUNTER_BYTES) */
+
+/*
+ * Every call that keeps split-K arrival counters (the balanced split, the
+ * producer/consumer split and the multi-token balanced split) keeps them in
+ * the first PKV_WORKSPACE_COUNTER_BYTES bytes of its workspace, or in the
+ * whole workspace when that is smaller.  Those bytes must be zero when the
+ * call's kernel starts; each call leaves them zero again unless it flagged
+ * PKV_ERRBIT_TIMEOUT or PKV_ERRBIT_WORKSPACE; paged_decode_workspace_clear
+ * zeroes them.  A kernel that meets a counter holding a value no zeroed
+ * workspace can produce sets PKV_ERRBIT_WORKSPACE.  That is certain when the
+ * stale value is negative or at least the number of pieces counted on it
+ * (a float's or a pointer's bit pattern, -1); a small positive stale value
+ * is caught only when a piece arrives before the early merge it causes.
+ * After the flag the results of the sequences whose split was counted are
+ * unspecified (some may be left unwritten); nothing faults or waits on a
+ * count, and the caller clears the counters before the next call.  The rest
+ * of a workspace is written before it is read within a call.
+ */
+#define PKV_WORKSPACE_COUNTER_BYTES 65536
 
 /*
  * Slot-mapped append ("Distributed LLM Inference Serving Platform", section
@@ -152,10 +174,12 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
  *  workspace      device scratch of at least the planned bytes (256-byte
  *                 aligned), may be NULL when the plan needs 0 bytes; the
  *                 caller owns it; calls that overlap in time need separate
- *                 workspaces.  It must be zero-filled before its first use:
- *                 the balanced split keeps per-segment arrival counters at
- *                 its start, and every call leaves them zero again (after a
- *                 call that flagged PKV_ERRBIT_TIMEOUT, zero it once more)
+ *                 workspaces.  Its first PKV_WORKSPACE_COUNTER_BYTES bytes
+ *                 must be zero before its first use (a whole zero-filled
+ *                 workspace will do): the balanced split keeps per-segment
+ *                 arrival counters there, and every call leaves them zero
+ *                 again (after a call that flagged PKV_ERRBIT_TIMEOUT or
+ *                 PKV_ERRBIT_WORKSPACE, zero them once more)
  *  lse_out        device fp32 [num_seqs][n_q_heads] natural-log sum of
  *                 exp(logits), may be NULL
  *  err_word       device int32, may be NULL (see the header comment)
@@ -249,8 +273,8 @@ int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_
  * pass would only add work.  The environment variable PKV_PREFIX_PASS=shared
  * (or =regular), read at every call, fixes the choice.
  * paged_decode_prefix_shared_plan gives the workspace bytes (for whichever
- * path the call takes); the workspace must be zero-filled before first use,
- * as for the balanced split.  pkv_bm_prefix_groups (pagedkv_blocks.h)
+ * path the call takes); its counter bytes (PKV_WORKSPACE_COUNTER_BYTES) must
+ * be zero before first use, as for the balanced split.  pkv_bm_prefix_groups (pagedkv_blocks.h)
  * derives the groups from the library's block manager.
  */
 int paged_decode_prefix_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
@@ -287,8 +311,9 @@ int paged_decode_attention_prefix_shared(
  * Requirements: head_dim % 16 == 0 for the append; the attention runs on the
  * balanced split only (head_dim 64 or 128, n_q/n_kv in {1, 2, 4, 8},
  * block_size a multiple of 16, at most 2048 sequences; PKV_ERR_UNSUPPORTED
- * otherwise).  paged_decode_plan_fp8 gives its workspace bytes; the
- * workspace must be zero-filled before its first use, as for the fp16 call.
+ * otherwise).  paged_decode_plan_fp8 gives its workspace bytes; its counter
+ * bytes (PKV_WORKSPACE_COUNTER_BYTES) must be zero before its first use, as
+ * for the fp16 call.
  * Pointers, errors and ownership as for the fp16 calls.
  */
 int paged_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
@@ -348,7 +373,8 @@ int paged_decode_attention_fp8_ex(void *out, const void *q, const void *k_cache,
  * byte per value (num_groups * max_prefix_len * n_kv_heads * head_dim * 2
  * bytes); below it, or with no group of two, the call runs
  * paged_decode_attention_fp8.  paged_decode_prefix_shared_plan_fp8 gives the
- * workspace bytes; the workspace must be zero-filled before its first use.
+ * workspace bytes; its counter bytes (PKV_WORKSPACE_COUNTER_BYTES) must be
+ * zero before its first use.
  * Groups, arguments, requirements and errors as for the two calls above.
  */
 int paged_decode_prefix_shared_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads,
@@ -394,9 +420,10 @@ int paged_decode_attention_prefix_shared_fp8_ex(
  * max_q_len * (n_q_heads / n_kv_heads) <= 16 and num_seqs <= 1024, the call
  * runs the balanced split of paged_decode_attention with every segment's
  * query rows -- the (token, head) pairs of its n_b tokens -- in one tile: the
- * workspace then holds arrival counters and must be zero-filled before its
- * first use, which every call leaves zeroed (after a call that flagged
- * PKV_ERRBIT_TIMEOUT, zero it once more).  Otherwise it runs fixed partitions,
+ * workspace then holds arrival counters (PKV_WORKSPACE_COUNTER_BYTES), which
+ * must be zero before its first use and which every call leaves zeroed (after
+ * a call that flagged PKV_ERRBIT_TIMEOUT or PKV_ERRBIT_WORKSPACE, zero them
+ * once more).  Otherwise it runs fixed partitions,
  * whose workspace (0 bytes when one partition covers max_context_len) needs
  * no zero-fill.  paged_decode_multi_plan gives the partition size (0 for the
  * balanced split) and the workspace bytes.
@@ -452,17 +479,18 @@ int paged_decode_attention_multi_ex(void *out, const void *q, const void *k_cach
  *  - Returns PKV_ERR_WORKSPACE, launching nothing, when the problem's split
  *    needs more than the array holds: more than PKV_NOALLOC_SCRATCH_BYTES
  *    for the balanced split (partition_tokens 0, whose need paged_decode_plan
- *    reports), or more than PKV_NOALLOC_SCRATCH_BYTES - 64 KiB for fixed
- *    partitions (a larger partition_tokens lowers their need).
+ *    reports), or more than PKV_NOALLOC_SCRATCH_BYTES -
+ *    PKV_WORKSPACE_COUNTER_BYTES for fixed partitions (a larger
+ *    partition_tokens lowers their need).
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and caches it; make that
  *    first call before any stream capture on that device.
- *  - The array's first 64 KiB hold the balanced split's arrival counters,
- *    which must be zero when its kernel starts.  Each balanced call clears
- *    them on cuda_stream first (cudaMemsetAsync, which allocates nothing), so
- *    neither a fixed-partition call nor a call that flagged
- *    PKV_ERRBIT_TIMEOUT leaves stale counts for the next one; fixed-partition
- *    plans keep their partial sums after those 64 KiB.  Every other byte is
+ *  - The array's first PKV_WORKSPACE_COUNTER_BYTES bytes hold the balanced
+ *    split's arrival counters, which must be zero when its kernel starts.
+ *    Each balanced call clears them on cuda_stream first (cudaMemsetAsync,
+ *    which allocates nothing), so neither a fixed-partition call nor a call
+ *    that flagged PKV_ERRBIT_TIMEOUT leaves stale counts for the next one;
+ *    fixed-partition plans keep their partial sums after those bytes.  Every other byte is
  *    written before it is read within a call.
  *  - All calls share the one array, and it keeps the last call's contents.
  *    Calls whose kernels overlap in time on the GPU (on different streams,
@@ -477,6 +505,17 @@ int paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache
                                    int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                                    int max_context_len, int partition_tokens, float *lse_out,
                                    int32_t *err_word, void *cuda_stream);
+
+/*
+ * Zeroes the arrival counters of a workspace on cuda_stream: the first
+ * min(workspace_bytes, PKV_WORKSPACE_COUNTER_BYTES) bytes (one
+ * cudaMemsetAsync; no allocation, no host wait, so it may be captured in a
+ * CUDA graph).  Call it once on a new workspace and after a call that
+ * flagged PKV_ERRBIT_TIMEOUT or PKV_ERRBIT_WORKSPACE.  workspace may be NULL
+ * only when workspace_bytes is 0 (a no-op).  Returns PKV_ERR_INVALID_ARG for
+ * a NULL workspace with bytes, PKV_ERR_CUDA when the memset fails.
+ */
+int paged_decode_workspace_clear(void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
  * Reads the device error word: waits for cuda_stream, copies *err_word to the

@@ -11,7 +11,9 @@ from .binding import (  # noqa: F401
     PKV_ERRBIT_CONTEXT,
     PKV_ERRBIT_SLOT,
     PKV_ERRBIT_TIMEOUT,
+    PKV_ERRBIT_WORKSPACE,
     PKV_TABLES_READY,
+    PKV_WORKSPACE_COUNTER_BYTES,
     PagedKVError,
     decode_plan,
     decode_plan_fp8,
@@ -28,6 +30,7 @@ from .binding import (  # noqa: F401
     paged_kv_append,
     paged_kv_append_fp8,
     paged_decode_step,
+    paged_decode_workspace_clear,
     prefix_shared_plan,
     prefix_shared_plan_fp8,
     status_string,

@@ -29,6 +29,10 @@ PKV_ERRBIT_BLOCK_ID = 0x1
 PKV_ERRBIT_SLOT = 0x2
 PKV_ERRBIT_CONTEXT = 0x4
 PKV_ERRBIT_TIMEOUT = 0x8
+PKV_ERRBIT_WORKSPACE = 0x10
+# bytes at the start of a workspace that hold arrival counters and must be
+# zero when a call starts
+PKV_WORKSPACE_COUNTER_BYTES = 65536
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +76,8 @@ def library():
         lib.paged_decode_attention.restype = c.c_int
         lib.paged_decode_attention_ex.argtypes = lib.paged_decode_attention.argtypes + [c.c_uint32]
         lib.paged_decode_attention_ex.restype = c.c_int
+        lib.paged_decode_workspace_clear.argtypes = [p, c.c_size_t, p]
+        lib.paged_decode_workspace_clear.restype = c.c_int
         lib.paged_kv_get_error.argtypes = [p, p, c.POINTER(c.c_int32)]
         lib.paged_kv_get_error.restype = c.c_int
         lib.paged_kv_status_string.argtypes = [c.c_int]
@@ -255,6 +261,17 @@ def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_le
                 _stream_handle(dev))
     _check("paged_decode_attention_noalloc", rc)
     return out
+
+
+def paged_decode_workspace_clear(workspace: torch.Tensor):
+    """Zero a workspace's arrival counters on the current stream (needed after a
+    call flagged PKV_ERRBIT_TIMEOUT or PKV_ERRBIT_WORKSPACE)."""
+    _need(workspace, "workspace", torch.uint8)
+    with torch.cuda.device(workspace.device):
+        _check("paged_decode_workspace_clear",
+               library().paged_decode_workspace_clear(
+                   _ptr(workspace) if workspace.numel() else None, workspace.numel(),
+                   _stream_handle(workspace.device)))
 
 
 def get_error(err_word: torch.Tensor) -> int:

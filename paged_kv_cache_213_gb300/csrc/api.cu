@@ -914,6 +914,16 @@ int paged_decode_attention_multi(void *out, const void *q, const void *k_cache,
                                            err_word, cuda_stream, 0);
 }
 
+int paged_decode_workspace_clear(void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    if (workspace_bytes == 0) return PKV_OK;
+    if (!workspace) return PKV_ERR_INVALID_ARG;
+    const size_t n = workspace_bytes < pkv::kBalancedCounterBytes ? workspace_bytes
+                                                                  : pkv::kBalancedCounterBytes;
+    return cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits_out) {
     if (!err_word) return PKV_ERR_INVALID_ARG;
     int32_t host = 0;

@@ -16,7 +16,8 @@
 // writes the output and resets the counter to zero -- there is no second
 // kernel.  The counters live at the start of the caller's workspace, which
 // must therefore be zero-filled before its first use; every call leaves them
-// zero again.
+// zero again, and an arrival that proves a counter did not start at zero
+// flags PKV_ERRBIT_WORKSPACE.
 //
 // The 16 rows of a segment's mma.m16n8k16 are its query rows.  For decode
 // (MT = false) they are the G query heads of KV head j (rows past G are
@@ -586,7 +587,13 @@ __global__ void __launch_bounds__(kW * 32, kW == kWSmall ? 3 : 1)
         // lane 1 counts: lane 0 issues the ring's TMA loads, and a release by
         // the lane that issued them could wait for them to land
         int old = 0;
-        if (lane == 1) old = atomic_add_acq_rel_gpu(&counters[wf], 1);
+        if (lane == 1) {
+            old = atomic_add_acq_rel_gpu(&counters[wf], 1);
+            if (counter_not_zeroed(old, wl - wf)) {
+                flag_error(a.err, PKV_ERRBIT_WORKSPACE);
+                atomic_exch_relaxed_gpu(&counters[wf], kCounterPoison);
+            }
+        }
         old = __shfl_sync(0xffffffffu, old, 1);
         __syncwarp();  // lane 1's acquire before lane 0's bulk copies of the records
         ++piece_no;
@@ -657,7 +664,8 @@ __global__ void __launch_bounds__(kW * 32, kW == kWSmall ? 3 : 1)
             }
             __syncwarp();  // before the next round overwrites the staged records
         }
-        if (lane == 0) store_relaxed_gpu(&counters[wf], 0);  // ready for the next call
+        // ready for the next call: back from n to 0 (a poisoned count stays >= n)
+        if (lane == 0) red_add_relaxed_gpu(&counters[wf], -(wl - wf + 1));
         if constexpr (MT) write_out_mt(b, j, M, Lsum, Mh, Lh);
         else write_out(b, j, M, Lsum);
         return true;

@@ -38,7 +38,8 @@
 //    all records of the segment in CTA order, writes the output and resets
 //    the counter.  No global round trip stalls a warp before its range is
 //    done, so no warp holds the ring up.  The counters sit at the start of
-//    the workspace and must be zero when the kernel starts.  Every unit's rows
+//    the workspace and must be zero when the kernel starts (an arrival that
+//    proves otherwise flags PKV_ERRBIT_WORKSPACE).  Every unit's rows
 //    are summed in the same order on every run, so results are reproducible
 //    bit for bit.
 //
@@ -450,7 +451,8 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
             }
             __syncwarp();  // every lane's reads before the next batch lands
         }
-        if (lane == 0) store_relaxed_gpu(&counters[first * HK + j], 0);  // ready for the next call
+        // ready for the next call: back from n to 0 (a poisoned count stays >= n)
+        if (lane == 0) red_add_relaxed_gpu(&counters[first * HK + j], -(last - first + 1));
         write_out(hg, b, M, L);
         return true;
     };
@@ -473,7 +475,13 @@ __global__ void __launch_bounds__(PipeCfg<D, G, HK>::THREADS, PipeCfg<D, G, HK>:
             for (int i = 0; i < pend_n; ++i) {
                 const int s0 = pend_hg[i] * T + s_pre[pend_b[i]];
                 const int nt = s_pre[pend_b[i] + 1] - s_pre[pend_b[i]];
-                if (old[i] == (s0 + nt - 1) / U - s0 / U) last_on |= 1 << i;
+                const int last = (s0 + nt - 1) / U - s0 / U;
+                if (old[i] == last) last_on |= 1 << i;
+                if (counter_not_zeroed(old[i], last)) {
+                    flag_error(a.err, PKV_ERRBIT_WORKSPACE);
+                    const int first = s0 / U;
+                    atomic_exch_relaxed_gpu(&counters[first * HK + j], kCounterPoison);
+                }
             }
         }
         last_on = __shfl_sync(0xffffffffu, last_on, 1);

@@ -8,6 +8,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "pagedkv.h"
+
 namespace pkv {
 
 // Launch with the programmatic stream-serialization attribute, so that the
@@ -111,11 +113,32 @@ struct DecodeArgs {
 int test_wait_polls();
 
 // The balanced kernel's workspace starts with one int32 arrival counter per
-// worker slot, kBalancedCounterBytes in all, whatever the plan.  They must be
-// zero when a launch starts; every launch leaves them zero again unless it
-// flagged PKV_ERRBIT_TIMEOUT.
+// worker slot, kBalancedCounterBytes in all, whatever the plan (the
+// producer/consumer kernel keeps its counters there too).  They must be zero
+// when a launch starts.  Each of the n pieces of a cut segment adds 1 to the
+// segment's counter; the one that sees n - 1 merges, then subtracts n (a
+// reduction without a result, which the warp does not wait for), so a
+// correct launch leaves the counter zero.  An arrival that sees a value >= n
+// (unsigned) proves that the counter did not start at zero: it flags
+// PKV_ERRBIT_WORKSPACE and sets the counter to kCounterPoison, which every
+// later arrival, in this launch and the next ones, also sees as >= n, even
+// after a merge's subtraction.  A stale start c is thus always caught when it
+// is negative or >= n (the first arrival sees c).  A c in [1, n) lets the
+// arrival that sees n - 1 merge early; it is caught when another piece
+// arrives before that merge's subtraction, and missed otherwise.
 constexpr int kBalancedMaxWorkers = 16384;
 constexpr size_t kBalancedCounterBytes = static_cast<size_t>(kBalancedMaxWorkers) * 4;
+static_assert(kBalancedCounterBytes == PKV_WORKSPACE_COUNTER_BYTES,
+              "the header states the counter region's size");
+constexpr int kCounterPoison = 1 << 30;
+static_assert(2 * kBalancedMaxWorkers < kCounterPoison,
+              "a poisoned count stays >= n after a merge subtracts n");
+
+// True when an arrival that saw `old` on a counter of `last + 1` pieces
+// proves that the counter did not start at zero.
+__host__ __device__ inline bool counter_not_zeroed(int old, int last) {
+    return static_cast<unsigned>(old) > static_cast<unsigned>(last);
+}
 
 // Workspace carve-up shared by the planner and the launcher.
 struct WorkspaceLayout {

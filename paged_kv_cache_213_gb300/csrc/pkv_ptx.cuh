@@ -236,8 +236,17 @@ __device__ __forceinline__ int atomic_add_relaxed_gpu(int *p, int v) {
     return old;
 }
 
-__device__ __forceinline__ void store_relaxed_gpu(int *p, int v) {
-    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Atomic add at GPU scope with no ordering of its own and no result, so the
+// issuing warp neither waits for it nor holds its registers for it.
+__device__ __forceinline__ void red_add_relaxed_gpu(int *p, int v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Exchange at GPU scope with no ordering of its own; returns the old value.
+__device__ __forceinline__ int atomic_exch_relaxed_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.relaxed.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 }  // namespace pkv

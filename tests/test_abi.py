@@ -39,6 +39,36 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(raw, n), f"{n} not exported"
 
 
+def header_defines():
+    """Integer #defines of include/pagedkv.h, by name."""
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    out = {}
+    for name, expr in re.findall(r"^#define\s+(PKV_\w+)\s+([(0-9][^/\n]*)", text, flags=re.M):
+        expr = re.sub(r"(\d)u\b", r"\1", expr.strip())
+        assert re.fullmatch(r"[0-9a-fA-Fx()<\s]+", expr), expr
+        out[name] = int(eval(expr))  # digits, parentheses and shifts only
+    return out
+
+
+def test_python_constants_match_the_header():
+    d = header_defines()
+    for name in ("PKV_ERRBIT_BLOCK_ID", "PKV_ERRBIT_SLOT", "PKV_ERRBIT_CONTEXT",
+                 "PKV_ERRBIT_TIMEOUT", "PKV_ERRBIT_WORKSPACE", "PKV_TABLES_READY",
+                 "PKV_WORKSPACE_COUNTER_BYTES"):
+        assert getattr(pkv, name) == d[name], name
+    bits = [d[n] for n in d if n.startswith("PKV_ERRBIT_")]
+    assert len(bits) == 5 and sum(bits) == 0x1f  # distinct single bits
+    assert d["PKV_NOALLOC_SCRATCH_BYTES"] == 16 << 20
+    assert d["PKV_WORKSPACE_COUNTER_BYTES"] < d["PKV_NOALLOC_SCRATCH_BYTES"]
+
+
+def test_workspace_clear_host_checks(lib):
+    """Zero bytes is a no-op and a NULL workspace with bytes is rejected, both
+    before any CUDA call."""
+    assert lib.paged_decode_workspace_clear(None, 0, None) == 0
+    assert lib.paged_decode_workspace_clear(None, 4096, None) == -1
+
+
 def test_status_strings(lib):
     assert pkv.status_string(0) == "ok"
     for s in (-1, -2, -3, -4, -5):

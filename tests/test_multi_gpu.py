@@ -235,6 +235,28 @@ def test_balanced_split_timeout_recovers(monkeypatch):
     assert_close(out, ref, what="after the timeout")
 
 
+def test_balanced_split_stale_counters_flagged():
+    """A workspace of 0xFF bytes (counters -1) on the multi-token balanced
+    split: the call returns with PKV_ERRBIT_WORKSPACE (the counters are only
+    counted, never waited on); after paged_decode_workspace_clear a call
+    matches the oracle."""
+    rng = np.random.default_rng(85)
+    lens = rng.integers(100, 3000, 32)
+    batch, q, qs = _problem(lens, [4] * 32, 32, 8, 128, 16, 86)
+    assert _balanced(batch, qs, 4)
+    _, ws = pkv.multi_plan(32, int(qs[-1]), 4, 32, 8, 128, 16, batch.max_blocks_per_seq,
+                           batch.max_context_len, 0)
+    work = torch.full((ws,), 0xFF, dtype=torch.uint8, device="cuda")
+    _, _, bits = _run_into(batch, q, qs, 4, workspace=work)
+    torch.cuda.synchronize()
+    assert bits == pkv.PKV_ERRBIT_WORKSPACE, bits
+    pkv.paged_decode_workspace_clear(work)
+    out, _, bits = _run_into(batch, q, qs, 4, workspace=work)
+    assert bits == 0
+    ref, _ = _oracle(batch, q, qs)
+    assert_close(out, ref, what="after the clear")
+
+
 def test_tables_ready_flag():
     """paged_decode_attention_multi_ex with PKV_TABLES_READY (lengths, tables
     and query_start read before the dependency wait), back to back:
