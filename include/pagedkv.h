@@ -274,8 +274,8 @@ int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_
  * (or =regular), read at every call, fixes the choice.
  * paged_decode_prefix_shared_plan gives the workspace bytes (for whichever
  * path the call takes); its counter bytes (PKV_WORKSPACE_COUNTER_BYTES) must
- * be zero before first use, as for the balanced split.  pkv_bm_prefix_groups (pagedkv_blocks.h)
- * derives the groups from the library's block manager.
+ * be zero before first use, as for the balanced split.  pkv_bm_prefix_groups
+ * (pagedkv_blocks.h) derives the groups from the library's block manager.
  */
 int paged_decode_prefix_shared_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                                     int block_size, int max_blocks_per_seq, int max_context_len,
