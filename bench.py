@@ -367,6 +367,9 @@ class Path:
         # launch flags of the attention call (PKV_TABLES_READY where the caller
         # knows that the kernel before writes no lengths or tables)
         self.attn_flags = 0
+        # flags of the one-call step (paged_decode_step_ex); see set_step_flags
+        self.step_flags = 0
+        self._sizes = (B, H, Hk, D, bs, MB, mcl)
         self.copies = [first] + [{k: v.clone() for k, v in first.items()}
                                  for _ in range(copies - 1)]
         for c in self.copies:
@@ -409,6 +412,21 @@ class Path:
                                        out=c["out"], workspace=ws, err_word=c["err"],
                                        flags=self.attn_flags)
 
+    def fused_step(self):
+        """The step is one paged_decode_step call (fp16, one query token, an
+        append, no prefix groups), which takes step flags."""
+        return self.has_append and not self.fp8 and self.groups is None
+
+    def set_step_flags(self, flags):
+        """Flags of the one-call step; the launch count follows the library's
+        own answer for these sizes and flags."""
+        if not self.fused_step():
+            return
+        self.step_flags = flags
+        B, H, Hk, D, bs, MB, mcl = self._sizes
+        self.step_launches = self.pkv.step_launches(B, H, Hk, D, bs, MB, mcl, self.P,
+                                                    num_tokens=B, flags=flags)
+
     def flaggable(self):
         """The attention call takes launch flags (every entry point here has
         an _ex form)."""
@@ -416,8 +434,9 @@ class Path:
 
     def step(self, i):
         """append + attention: one library call when the step has an append on
-        the default (fp16, one query token) path, so that the attention's
-        prologue overlaps the append."""
+        the default (fp16, one query token) path: under PKV_APPEND_NEWEST one
+        kernel that also appends, otherwise the append kernel with the
+        attention's prologue overlapping it."""
         pkv, bt, c = self.pkv, self.batch, self.copies[i]
         if not self.has_append:
             self.attend(i)
@@ -436,7 +455,7 @@ class Path:
                               bt.block_size, max_context_len=bt.max_context_len,
                               partition_tokens=self.P, out=c["out"],
                               workspace=c["work"] if self.ws_bytes > 0 else None,
-                              err_word=c["err"])
+                              err_word=c["err"], flags=self.step_flags)
 
     def errors(self):
         return [self.pkv.get_error(c["err"]) for c in self.copies]
@@ -676,6 +695,13 @@ def run_ours(args):
     has_append = path.has_append
     B, H, Hk, D, bs = batch.num_seqs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, \
         batch.block_size
+    # The step's promises, both true of a decode loop: token b is sequence b's
+    # newest token (so the attention kernel appends it itself, in one launch),
+    # and the kernel before the step (here the previous step) writes no
+    # lengths, tables or slot mapping.  The same steps without the flags (the
+    # append kernel, then the attention) are timed too (ms_per_step_plain_call).
+    step_flags = pkv.PKV_APPEND_NEWEST | pkv.PKV_TABLES_READY
+    path.set_step_flags(step_flags)
     timer = Timer(torch, device, args.graph_steps)
 
     # The end-to-end leg: each input copy's per-step inputs live as
@@ -742,6 +768,11 @@ def run_ours(args):
         path.attn_flags = pkv.PKV_TABLES_READY
     attn_ms = timer.back_to_back(lambda i: path.attend(i % ROTATE), args.steps)
     path.attn_flags = 0
+    step_plain = None
+    if path.fused_step():
+        path.set_step_flags(0)
+        step_plain = timer.back_to_back(lambda i: path.step(i % ROTATE), args.steps)
+        path.set_step_flags(step_flags)
     step_iso = timer.isolated(lambda i: path.step(i % ROTATE), args.steps)
     attn_iso = timer.isolated(lambda i: path.attend(i % ROTATE), args.steps)
     clocks = sampler.stop()
@@ -776,7 +807,8 @@ def run_ours(args):
                "value_isolated": round(e2e_iso_val, 2),
                "ms_per_step_isolated": round(e2e_iso_ms, 5),
                "timing": "every step: pinned-host -> device copy of the step's inputs, the step "
-                         "(paged_decode_step), device -> pinned-host copy of out; steps back to "
+                         "(paged_decode_step with the step flags), device -> pinned-host copy "
+                         "of out; steps back to "
                          "back over the four input copies (value), or each its own timed region "
                          "after an L2 flush (value_isolated)"}
 
@@ -828,6 +860,9 @@ def run_ours(args):
         "attention_flags": "PKV_TABLES_READY" if attn_plain is not None else "none",
         "attention_ms_plain_call": round(statistics.fmean(attn_plain), 5)
         if attn_plain is not None else None,
+        "step_flags": "PKV_APPEND_NEWEST|PKV_TABLES_READY" if path.fused_step() else "none",
+        "ms_per_step_plain_call": round(statistics.fmean(step_plain), 5)
+        if step_plain is not None else None,
         "ms_per_step_isolated": round(statistics.fmean(step_iso), 5),
         "attention_ms_isolated": round(attn_iso_mean, 5),
         "percentiles_ms": {"step": pcts(step_ms_list), "attention": pcts(attn_ms),
@@ -855,7 +890,8 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": per_call * n_calls,
         "gpu_launches_note": f"{per_call} launch(es) per step (the append when the step has "
-                             "one, then the attention: one balanced kernel, or partition + "
+                             "one and the attention does not do it under PKV_APPEND_NEWEST, "
+                             "then the attention: one balanced kernel, or partition + "
                              "merge kernels, or the shared-prefix pass + suffix pass), times "
                              "the timed steps of `value`; the other timing passes (attention "
                              "alone, isolated calls, eager, e2e, per_config) launch more",

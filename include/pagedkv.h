@@ -84,6 +84,8 @@ typedef enum pkv_status {
 #define PKV_ERRBIT_TIMEOUT 0x8  /* a bounded wait for a block copy gave up */
 #define PKV_ERRBIT_WORKSPACE 0x10 /* an arrival counter of the workspace did not
                                      start at zero (see PKV_WORKSPACE_COUNTER_BYTES) */
+#define PKV_ERRBIT_APPEND 0x20  /* under PKV_APPEND_NEWEST, a token that is not its
+                                   sequence's newest (see paged_decode_step_ex) */
 
 /*
  * Every call that keeps split-K arrival counters (the balanced split, the
@@ -238,6 +240,57 @@ int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_
                       int n_kv_heads, int head_dim, int block_size, int max_context_len,
                       int partition_tokens, void *workspace, size_t workspace_bytes,
                       float *lse_out, int32_t *err_word, void *cuda_stream);
+
+/*
+ * paged_decode_step with flags.  The pages have no counterpart: this is how
+ * one decode step runs as one kernel.
+ *  PKV_APPEND_NEWEST  the caller guarantees that num_tokens == num_seqs and
+ *                     that token b is sequence b's newest token:
+ *                     slot_mapping[b] is the slot of position
+ *                     context_lens[b] - 1 of sequence b (block
+ *                     block_tables[b][(L - 1) / block_size], row
+ *                     (L - 1) % block_size), or negative for no token.  The
+ *                     attention kernel then does the append itself: the warp
+ *                     that loads a sequence's last 16-token tile writes the
+ *                     token's K/V rows to the cache and into that tile, so no
+ *                     append kernel runs and no wait for one.  Results and
+ *                     cache contents are those of paged_decode_step.  A token
+ *                     whose slot is not its sequence's newest position, or
+ *                     that belongs to an empty sequence, sets
+ *                     PKV_ERRBIT_APPEND; the former is still written to its
+ *                     slot, but the results of any sequence that reads that
+ *                     slot are then unspecified.
+ *  PKV_TABLES_READY   with PKV_APPEND_NEWEST, as for
+ *                     paged_decode_attention_ex, where the kernel before
+ *                     also writes no slot_mapping: the step's prologue runs
+ *                     while that kernel drains.
+ * The flags take effect where the step runs the balanced split on per-warp
+ * ranges (block_size a multiple of 16, partition_tokens 0, batches of few
+ * (sequence, KV head) segments); elsewhere the call is paged_decode_step.
+ * Other flag bits are rejected with PKV_ERR_INVALID_ARG.
+ */
+#define PKV_APPEND_NEWEST 0x2u
+int paged_decode_step_ex(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                         int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                         int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
+                         int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                         int partition_tokens, void *workspace, size_t workspace_bytes,
+                         float *lse_out, int32_t *err_word, void *cuda_stream, uint32_t flags);
+
+/*
+ * How many kernels paged_decode_step_ex launches for these sizes and flags
+ * (host only; the automatic split queries the current device, as
+ * paged_decode_plan does): the append unless the attention does it
+ * (PKV_APPEND_NEWEST on per-warp ranges), then one attention kernel, or two
+ * for fixed partitions with a merge.  *launches_out (host) receives it.
+ * Returns the status that paged_decode_plan would, or PKV_ERR_INVALID_ARG
+ * for unknown flag bits.
+ */
+int paged_decode_step_launches(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                               int block_size, int max_blocks_per_seq, int max_context_len,
+                               int partition_tokens, int num_tokens, uint32_t flags,
+                               int *launches_out);
 
 /*
  * Prefix-aware (cascade) decode attention ("Distributed LLM Inference Serving

@@ -12,7 +12,9 @@ from .binding import (  # noqa: F401
     PKV_ERRBIT_SLOT,
     PKV_ERRBIT_TIMEOUT,
     PKV_ERRBIT_WORKSPACE,
+    PKV_ERRBIT_APPEND,
     PKV_TABLES_READY,
+    PKV_APPEND_NEWEST,
     PKV_WORKSPACE_COUNTER_BYTES,
     PagedKVError,
     decode_plan,
@@ -34,4 +36,5 @@ from .binding import (  # noqa: F401
     prefix_shared_plan,
     prefix_shared_plan_fp8,
     status_string,
+    step_launches,
 )

@@ -30,6 +30,7 @@ PKV_ERRBIT_SLOT = 0x2
 PKV_ERRBIT_CONTEXT = 0x4
 PKV_ERRBIT_TIMEOUT = 0x8
 PKV_ERRBIT_WORKSPACE = 0x10
+PKV_ERRBIT_APPEND = 0x20
 # bytes at the start of a workspace that hold arrival counters and must be
 # zero when a call starts
 PKV_WORKSPACE_COUNTER_BYTES = 65536
@@ -155,6 +156,7 @@ def decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_block
 
 
 PKV_TABLES_READY = 0x1
+PKV_APPEND_NEWEST = 0x2  # paged_decode_step: token b is sequence b's newest (one launch)
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, n_q_heads,
@@ -521,6 +523,22 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, 
 # multi-token (causal) attention: speculative verify, chunked prefill
 # ---------------------------------------------------------------------------
 
+def step_launches(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                  max_context_len=0, partition_tokens=0, num_tokens=None, flags=0):
+    """Kernels that paged_decode_step launches for these sizes and flags."""
+    lib = library()
+    fn = lib.paged_decode_step_launches
+    c = ctypes
+    fn.argtypes = [c.c_int] * 9 + [c.c_uint32, c.POINTER(c.c_int)]
+    fn.restype = c.c_int
+    n = ctypes.c_int(-1)
+    _check("paged_decode_step_launches",
+           fn(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+              int(max_context_len or 0), partition_tokens,
+              num_seqs if num_tokens is None else num_tokens, int(flags), ctypes.byref(n)))
+    return n.value
+
+
 def multi_plan(num_seqs, total_q, max_q_len, n_q_heads, n_kv_heads, head_dim, block_size,
                max_blocks_per_seq, max_context_len=0, partition_tokens=0):
     """(partition_tokens, workspace_bytes) of paged_decode_attention_multi."""
@@ -598,15 +616,18 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
 def paged_decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
                       context_lens, scale, n_q_heads, n_kv_heads, head_dim, block_size,
                       max_context_len=None, partition_tokens=0, out=None, workspace=None,
-                      lse=None, err_word=None):
+                      lse=None, err_word=None, flags=0):
     """paged_kv_append then paged_decode_attention in one call: the attention's
-    prologue overlaps the append.  Returns out [B, H, d] fp16."""
+    prologue overlaps the append.  flags (paged_decode_step_ex):
+    PKV_APPEND_NEWEST (token b is sequence b's newest: the attention kernel
+    appends it, one launch) and PKV_TABLES_READY.  Returns out [B, H, d] fp16."""
     lib = library()
-    fn = lib.paged_decode_step
+    fn = lib.paged_decode_step_ex
     c = ctypes
     p = c.c_void_p
     fn.argtypes = [p, p, p, c.c_int, p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float,
-                   c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p, p]
+                   c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p, c.c_size_t, p, p, p,
+                   c.c_uint32]
     fn.restype = c.c_int
     dev = q.device
     for t, name, dt in ((k_new, "k_new", torch.float16), (v_new, "v_new", torch.float16),
@@ -639,6 +660,6 @@ def paged_decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tab
                 _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, MB,
                 k_cache.shape[0], float(scale), n_q_heads, n_kv_heads, head_dim, block_size, mcl,
                 P, _ptr(workspace) if ws > 0 else None, workspace.numel() if ws > 0 else 0,
-                _ptr(lse), _ptr(err_word), _stream_handle(dev))
-    _check("paged_decode_step", rc)
+                _ptr(lse), _ptr(err_word), _stream_handle(dev), int(flags))
+    _check("paged_decode_step_ex", rc)
     return out

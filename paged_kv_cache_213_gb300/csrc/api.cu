@@ -171,14 +171,31 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
 
 namespace {
 
+// The step appends inside the attention kernel (one launch): the caller's
+// PKV_APPEND_NEWEST, one token per sequence, and per-warp balanced ranges.
+bool step_fuses(const Plan &plan, int num_seqs, int num_tokens, uint32_t flags) {
+    return (flags & PKV_APPEND_NEWEST) && num_tokens == num_seqs && num_seqs > 0 &&
+           plan.balanced && plan.bal.kind == 0;
+}
+
+// The decode step's new tokens, when the attention kernel does their append
+// (paged_decode_step_ex under PKV_APPEND_NEWEST).
+struct FusedAppend {
+    const void *k_new;
+    const void *v_new;
+    const int64_t *slot_mapping;
+};
+
 // paged_decode_attention; defer = 2 when this library's append was launched
-// just before on the same stream (the prologue may then run under it).
+// just before on the same stream (the prologue may then run under it).  With
+// fa, the plan must be the balanced split on per-warp ranges.
 int decode_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                           int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
                           int n_kv_heads, int head_dim, int block_size, int max_context_len,
                           int partition_tokens, void *workspace, size_t workspace_bytes,
-                          float *lse_out, int32_t *err_word, void *cuda_stream, int defer);
+                          float *lse_out, int32_t *err_word, void *cuda_stream, int defer,
+                          const FusedAppend *fa = nullptr);
 
 }  // namespace
 
@@ -221,6 +238,37 @@ int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_
                       int n_kv_heads, int head_dim, int block_size, int max_context_len,
                       int partition_tokens, void *workspace, size_t workspace_bytes,
                       float *lse_out, int32_t *err_word, void *cuda_stream) {
+    return paged_decode_step_ex(k_new, v_new, slot_mapping, num_tokens, out, q, k_cache, v_cache,
+                                block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                num_blocks, scale, n_q_heads, n_kv_heads, head_dim, block_size,
+                                max_context_len, partition_tokens, workspace, workspace_bytes,
+                                lse_out, err_word, cuda_stream, 0);
+}
+
+int paged_decode_step_launches(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                               int block_size, int max_blocks_per_seq, int max_context_len,
+                               int partition_tokens, int num_tokens, uint32_t flags,
+                               int *launches_out) {
+    if ((flags & ~(PKV_TABLES_READY | PKV_APPEND_NEWEST)) || num_tokens < 0)
+        return PKV_ERR_INVALID_ARG;
+    Plan plan{};
+    const int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, max_context_len, partition_tokens, &plan);
+    if (rc != PKV_OK) return rc;
+    const int attention = num_seqs == 0 ? 0 : (!plan.balanced && plan.ws_bytes > 0 ? 2 : 1);
+    const int append = num_tokens > 0 && !step_fuses(plan, num_seqs, num_tokens, flags) ? 1 : 0;
+    if (launches_out) *launches_out = attention + append;
+    return PKV_OK;
+}
+
+int paged_decode_step_ex(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                         int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                         int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
+                         int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                         int partition_tokens, void *workspace, size_t workspace_bytes,
+                         float *lse_out, int32_t *err_word, void *cuda_stream, uint32_t flags) {
+    if (flags & ~(PKV_TABLES_READY | PKV_APPEND_NEWEST)) return PKV_ERR_INVALID_ARG;
     // check the attention's arguments first so that a rejected call changes nothing
     Plan plan{};
     int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
@@ -229,6 +277,19 @@ int paged_decode_step(const void *k_new, const void *v_new, const int64_t *slot_
     if (num_seqs > 0 && plan.ws_bytes > 0 &&
         (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)))
         return PKV_ERR_WORKSPACE;
+    if (step_fuses(plan, num_seqs, num_tokens, flags)) {
+        // one kernel: the attention appends each sequence's newest token itself
+        if (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+            !aligned(slot_mapping, 8))
+            return PKV_ERR_INVALID_ARG;
+        const FusedAppend fa{k_new, v_new, slot_mapping};
+        return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens,
+                                     num_seqs, max_blocks_per_seq, num_blocks, scale, n_q_heads,
+                                     n_kv_heads, head_dim, block_size, max_context_len,
+                                     partition_tokens, workspace, workspace_bytes, lse_out,
+                                     err_word, cuda_stream,
+                                     (flags & PKV_TABLES_READY) ? 2 : 0, &fa);
+    }
     rc = paged_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens, n_kv_heads,
                          head_dim, block_size, num_blocks, err_word, cuda_stream);
     if (rc != PKV_OK) return rc;
@@ -248,7 +309,8 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
                           int max_blocks_per_seq, int64_t num_blocks, float scale, int n_q_heads,
                           int n_kv_heads, int head_dim, int block_size, int max_context_len,
                           int partition_tokens, void *workspace, size_t workspace_bytes,
-                          float *lse_out, int32_t *err_word, void *cuda_stream, int defer) {
+                          float *lse_out, int32_t *err_word, void *cuda_stream, int defer,
+                          const FusedAppend *fa) {
     if (num_blocks <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     Plan plan{};
     int rc = make_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
@@ -297,6 +359,12 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     a.max_parts = plan.max_parts;
     a.defer_dep_wait = plan.balanced ? defer : 0;
     a.first_wait_polls = pkv::test_wait_polls();
+    if (fa) {  // the caller checked the plan: balanced, per-warp ranges
+        a.append_k = fa->k_new;
+        a.append_v = fa->v_new;
+        a.append_slots = fa->slot_mapping;
+        a.fuse_append = 1;
+    }
     if (plan.balanced &&
         static_cast<long long>(num_blocks) * n_kv_heads * block_size >= (1LL << 31))
         return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit

@@ -244,6 +244,10 @@ __global__ void __launch_bounds__(kW * 32, kW == kWSmall ? 3 : 1)
             s_qs[b] = a.query_start[b];
         } else {
             s_len[b] = clamped_len(a, b, blockIdx.x == 0);
+            // fused append: a token of an empty sequence has no newest position
+            if (!F8 && a.fuse_append && blockIdx.x == 0 && s_len[b] == 0 &&
+                a.append_slots[b] >= 0)
+                flag_error(a.err, PKV_ERRBIT_APPEND);
         }
         s_skip[b] = 0;
     }
@@ -391,6 +395,23 @@ __global__ void __launch_bounds__(kW * 32, kW == kWSmall ? 3 : 1)
     int ids_cur = load_ids(0);
     int ids_next = load_ids(1);
 
+    // Fused append (fp16 decode only): per ring slot, this lane's 16-byte
+    // piece of the newest token's K row (lanes < D/8) or V row (the next D/8
+    // lanes), its slot and the tile's block id, fetched when a segment's last
+    // tile is issued and used when that tile is consumed.
+    constexpr bool kFuse = !MT && !F8;
+    constexpr int kU8 = D / 8;  // 16-byte pieces per row
+    uint4 app_piece[kS];
+    long long app_slot[kS];
+    int app_id[kS];
+#pragma unroll
+    for (int s = 0; s < kS; ++s) {
+        app_piece[s] = make_uint4(0u, 0u, 0u, 0u);
+        app_slot[s] = -1;
+        app_id[s] = -1;
+    }
+    auto is_last_tile = [&](const Cursor &c) { return c.t == s_pre[c.b + 1] - s_pre[c.b] - 1; };
+
     // All lanes call (the cursor bookkeeping is warp-uniform); lane 0 issues.
     auto issue = [&](int k) {
         const int slot = k % kS;
@@ -402,6 +423,21 @@ __global__ void __launch_bounds__(kW * 32, kW == kWSmall ? 3 : 1)
             ids_next = load_ids((k >> 5) + 1);
         }
         const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
+        if (kFuse && a.fuse_append && is_last_tile(pc)) {
+            const size_t row = static_cast<size_t>(pc.b) * Hk + pc.j;
+            uint4 piece = make_uint4(0u, 0u, 0u, 0u);
+            if (lane < 2 * kU8)
+                piece = __ldg(static_cast<const uint4 *>(lane < kU8 ? a.append_k : a.append_v) +
+                              row * kU8 + (lane % kU8));
+            const long long sl = a.append_slots[pc.b];
+#pragma unroll
+            for (int s = 0; s < kS; ++s)
+                if (s == slot) {
+                    app_piece[s] = piece;
+                    app_slot[s] = sl;
+                    app_id[s] = id;
+                }
+        }
         if (lane == 0) {
             uint64_t *bar = &full_bar[warp][slot];
             const int tok0 = (pc.t + s_skip[pc.b]) * kMmaTile;
@@ -713,6 +749,49 @@ __global__ void __launch_bounds__(kW * 32, kW == kWSmall ? 3 : 1)
         unsigned char *vs = ks + C::KV_BYTES;
         const int tok0 = (cc.t + s_skip[cc.b]) * kMmaTile;
         const int n_valid = s_ok[warp][slot] ? min(kMmaTile, s_len[cc.b] - tok0) : 0;
+        if (kFuse && a.fuse_append && is_last_tile(cc)) {
+            uint4 piece = make_uint4(0u, 0u, 0u, 0u);
+            long long sl = -1;
+            int tile_id = -1;
+#pragma unroll
+            for (int s = 0; s < kS; ++s)
+                if (s == slot) {
+                    piece = app_piece[s];
+                    sl = app_slot[s];
+                    tile_id = app_id[s];
+                }
+            if (sl >= 0) {
+                const int L = s_len[cc.b];
+                const long long newest = static_cast<long long>(tile_id) * bs + (L - 1) % bs;
+                if (sl == newest && n_valid > 0) {
+                    // row L - 1 of the staged tile takes the new token (the
+                    // 128B-swizzled layout of the TMA boxes, 64 columns each)
+                    const int r = L - 1 - tok0;
+                    if (lane < 2 * kU8) {
+                        const int u = lane % kU8;
+                        unsigned char *tile = lane < kU8 ? ks : vs;
+                        *reinterpret_cast<uint4 *>(tile + (u >> 3) * C::BOX_BYTES + swz(r, u & 7)) =
+                            piece;
+                    }
+                    fence_proxy_async_smem();  // before a later TMA write of this slot
+                    __syncwarp();
+                } else if (sl != newest && lane == 0) {
+                    flag_error(a.err, PKV_ERRBIT_APPEND);
+                }
+                // the append itself: the token's rows into its cache slot
+                if (sl < a.num_blocks * bs) {
+                    if (lane < 2 * kU8) {
+                        const long long dst =
+                            ((sl / bs) * Hk + cc.j) * static_cast<long long>(bs) + sl % bs;
+                        uint4 *cache = static_cast<uint4 *>(const_cast<void *>(
+                            lane < kU8 ? a.k_cache : a.v_cache));
+                        cache[dst * kU8 + (lane % kU8)] = piece;
+                    }
+                } else if (lane == 0 && cc.j == 0) {
+                    flag_error(a.err, PKV_ERRBIT_SLOT);
+                }
+            }
+        }
         if constexpr (MT) {
             mma_tile_multi<D>(ks, vs, n_valid, min(n_valid, max(0, lim_lo - tok0)),
                               min(n_valid, max(0, lim_hi - tok0)), qa, qh, a.scale_log2, o,

@@ -90,8 +90,10 @@ struct DecodeArgs {
     //     wait, which comes before the first read of those partials;
     //  2: the kernel before writes no lengths or tables (this library's
     //     append, or a caller's kernel under PKV_TABLES_READY): the prologue
-    //     (lengths, block ids, split) runs before the wait, which comes
-    //     before the first read of q, the caches or the workspace.
+    //     (lengths, block ids, split; under fuse_append also the check of
+    //     empty sequences' slots) runs before the wait, which comes before
+    //     the first read of q, the caches, the appended rows or the
+    //     workspace.
     int defer_dep_wait;
     // FP8 caches (balanced kernel only): k_cache / v_cache hold E4M3 codes,
     // scale_log2 already includes k_scale, and outputs are multiplied by v_scale
@@ -102,6 +104,16 @@ struct DecodeArgs {
     const int32_t *query_start = nullptr;
     int total_q = 0;
     int max_q_len = 0;            // host bound of n_b; a longer sequence is flagged
+    // The append inside the attention kernel (paged_decode_step under
+    // PKV_APPEND_NEWEST; fp16 caches, per-warp balanced split only): token b
+    // of append_k / append_v ([B][Hk][D] fp16) is sequence b's newest token,
+    // at slot append_slots[b] (negative: no token).  The warp that loads a
+    // segment's last tile writes the token's rows to the cache and into that
+    // tile in shared memory, so no separate append kernel runs before.
+    const void *append_k = nullptr;
+    const void *append_v = nullptr;
+    const int64_t *append_slots = nullptr;
+    int fuse_append = 0;
     // Test hook (the environment variable PKV_TEST_WAIT_POLLS, read at every
     // call): >= 0 makes each warp's first wait for K/V data give up after
     // that many non-blocking polls, so that the timeout path (flag, drain the

@@ -53,11 +53,12 @@ def header_defines():
 def test_python_constants_match_the_header():
     d = header_defines()
     for name in ("PKV_ERRBIT_BLOCK_ID", "PKV_ERRBIT_SLOT", "PKV_ERRBIT_CONTEXT",
-                 "PKV_ERRBIT_TIMEOUT", "PKV_ERRBIT_WORKSPACE", "PKV_TABLES_READY",
-                 "PKV_WORKSPACE_COUNTER_BYTES"):
+                 "PKV_ERRBIT_TIMEOUT", "PKV_ERRBIT_WORKSPACE", "PKV_ERRBIT_APPEND",
+                 "PKV_TABLES_READY", "PKV_APPEND_NEWEST", "PKV_WORKSPACE_COUNTER_BYTES"):
         assert getattr(pkv, name) == d[name], name
     bits = [d[n] for n in d if n.startswith("PKV_ERRBIT_")]
-    assert len(bits) == 5 and sum(bits) == 0x1f  # distinct single bits
+    assert len(bits) == 6 and sum(bits) == 0x3f  # distinct single bits
+    assert d["PKV_TABLES_READY"] & d["PKV_APPEND_NEWEST"] == 0
     assert d["PKV_NOALLOC_SCRATCH_BYTES"] == 16 << 20
     assert d["PKV_WORKSPACE_COUNTER_BYTES"] < d["PKV_NOALLOC_SCRATCH_BYTES"]
 
@@ -159,6 +160,26 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     mu.restype = c.c_int
     assert mu(fake, fake, fake, fake, fake, fake, fake, 4, 8, 2, 8, 40, 0.1, 8, 2, 128, 16, 0,
               0, fake, 1 << 20, n, n, n, 0x10) == -1
+    st = lib.paged_decode_step_ex
+    st.argtypes = [p_, p_, p_, c.c_int] + [p_] * 6 + [c.c_int, c.c_int, c.c_int64, c.c_float] + \
+        [c.c_int] * 6 + [p_, c.c_size_t, p_, p_, p_, c.c_uint32]
+    st.restype = c.c_int
+    for bad in (0x4, 0x10, 0x80000000):
+        assert st(fake, fake, fake, 4, fake, fake, fake, fake, fake, fake, 4, 8, 40, 0.1, 8, 2,
+                  128, 16, 0, 0, fake, 1 << 20, n, n, n, bad) == -1
+
+
+def test_step_launches_with_fixed_partitions(lib):
+    """The launch count of a step, for plans that need no device query: the
+    append, then one kernel (one partition) or two (partitions + merge)."""
+    # B=4, 8/2 heads, d=128, bs=16, 8 blocks per sequence: up to 128 tokens
+    assert pkv.step_launches(4, 8, 2, 128, 16, 8, 0, 64) == 3
+    assert pkv.step_launches(4, 8, 2, 128, 16, 8, 0, 128) == 2
+    assert pkv.step_launches(4, 8, 2, 128, 16, 8, 0, 64, num_tokens=0) == 2
+    # the fused append needs the balanced split: fixed partitions keep the append
+    assert pkv.step_launches(4, 8, 2, 128, 16, 8, 0, 128, flags=pkv.PKV_APPEND_NEWEST) == 2
+    with pytest.raises(pkv.PagedKVError):
+        pkv.step_launches(4, 8, 2, 128, 16, 8, 0, 128, flags=0x8)
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="a GPU is present")

@@ -393,3 +393,86 @@ def test_plain_call_after_a_kernel_that_rewrites_the_tables(what):
             max_context_len=batch.max_context_len, workspace=work, err_word=err)
         assert pkv.get_error(err) == 0
         assert_close(out.cpu().numpy(), ref["out"], what=f"after rewritten {what}")
+
+
+def _run_step(batch, flags, slot_mapping=None, context_lens=None):
+    """paged_decode_step on fresh device copies; numpy out, lse, caches, bits."""
+    dev = to_dev(batch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lse = torch.full((batch.num_seqs, batch.n_q_heads), float("nan"), device="cuda")
+    sm = dev["slot_mapping"] if slot_mapping is None else torch.from_numpy(slot_mapping).cuda()
+    cl = dev["context_lens"] if context_lens is None else torch.from_numpy(context_lens).cuda()
+    out = pkv.paged_decode_step(dev["k_new"], dev["v_new"], sm, dev["q"], dev["k_cache"],
+                                dev["v_cache"], dev["block_tables"], cl, batch.scale,
+                                batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
+                                batch.block_size, max_context_len=batch.max_context_len,
+                                lse=lse, err_word=err, flags=flags)
+    bits = pkv.get_error(err)
+    return (out.cpu().numpy(), lse.cpu().numpy(), dev["k_cache"].cpu().numpy(),
+            dev["v_cache"].cpu().numpy(), bits)
+
+
+def _same_bits(a, b):
+    return np.array_equal(np.ascontiguousarray(a).view(np.uint8),
+                          np.ascontiguousarray(b).view(np.uint8))
+
+
+FUSED = (pkv.PKV_APPEND_NEWEST, pkv.PKV_APPEND_NEWEST | pkv.PKV_TABLES_READY)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_fused_append_step_matches_two_kernel_step(cfg):
+    """PKV_APPEND_NEWEST: the attention kernel appends each sequence's newest
+    token itself (one launch).  Output, lse and the whole pool are bit-identical
+    to the two-kernel step, and the output matches the oracle."""
+    batch = wl.workload(cfg, poison=True)
+    ref = _run_step(batch, 0)
+    assert ref[4] == 0
+    for flags in FUSED:
+        got = _run_step(batch, flags)
+        assert got[4] == 0, flags
+        for x, y in zip(got[:4], ref[:4]):
+            assert _same_bits(x, y), flags
+    assert_close(ref[0], oracle_step(batch)["out"], what=f"workload {cfg} step")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_fused_append_step_edge_shapes(d, g, bs):
+    rng = np.random.default_rng(600 + d + 10 * g + bs)
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 64, 130, 300, 1000]
+    batch = wl.make_batch("fused", lens, 2 * g, 2, d, bs, rng, append=True, poison=True)
+    ref = _run_step(batch, 0)
+    assert ref[4] == 0
+    for flags in FUSED:
+        got = _run_step(batch, flags)
+        assert got[4] == 0
+        for x, y in zip(got[:4], ref[:4]):
+            assert _same_bits(x, y), (d, g, bs, flags)
+    assert_close(ref[0], oracle_step(batch)["out"], what=f"fused d={d} g={g} bs={bs}")
+
+
+def test_fused_append_padding_and_broken_promises():
+    rng = np.random.default_rng(611)
+    batch = wl.make_batch("fused-edge", [5, 40, 17, 100, 33], 8, 2, 128, 16, rng, append=True,
+                          poison=True, pool_extra=0.5)
+    used = set(batch.block_tables[b, i] for b in range(batch.num_seqs)
+               for i in range((int(batch.context_lens[b]) + 15) // 16))
+    free = next(i for i in range(batch.num_blocks) if i not in used)
+    sm = batch.slot_mapping.copy()
+    sm[1] = -1                  # no token for sequence 1
+    sm[2] = free * 16 + 3       # a token away from sequence 2's newest position
+    ref = _run_step(batch, 0, slot_mapping=sm)
+    assert ref[4] == 0
+    for flags in FUSED:
+        got = _run_step(batch, flags, slot_mapping=sm)
+        assert got[4] == pkv.PKV_ERRBIT_APPEND, got[4]   # only the broken promise
+        for x, y in zip(got[:4], ref[:4]):                # the token is still written
+            assert _same_bits(x, y), flags
+    # a token for an empty sequence is flagged and not written
+    cl = batch.context_lens.copy()
+    cl[3] = 0
+    got = _run_step(batch, pkv.PKV_APPEND_NEWEST, context_lens=cl)
+    assert got[4] == pkv.PKV_ERRBIT_APPEND
+    assert np.all(got[0][3] == 0) and np.all(np.isneginf(got[1][3]))

@@ -96,9 +96,21 @@ def test_fp16_random(seed):
                                         max_context_len=batch.max_context_len, err_word=err)
         flagged = pkv.paged_decode_attention(*args, max_context_len=batch.max_context_len,
                                              err_word=err, flags=pkv.PKV_TABLES_READY)
+        # the one-launch step (the attention appends the newest tokens itself)
+        dev2 = to_dev(batch)
+        args2 = (dev2["q"], dev2["k_cache"], dev2["v_cache"], dev2["block_tables"],
+                 dev2["context_lens"], batch.scale, g * hk, hk, d, bs)
+        fused = pkv.paged_decode_step(dev2["k_new"], dev2["v_new"], dev2["slot_mapping"],
+                                      *args2, max_context_len=batch.max_context_len,
+                                      err_word=err,
+                                      flags=pkv.PKV_APPEND_NEWEST | pkv.PKV_TABLES_READY)
         assert pkv.get_error(err) == 0
-        for o in (stepped, flagged):
+        for o in (stepped, flagged, fused):
             assert np.array_equal(o.cpu().numpy().view(np.uint16), auto.view(np.uint16))
+        assert np.array_equal(dev2["k_cache"].cpu().numpy().view(np.uint16),
+                              dev["k_cache"].cpu().numpy().view(np.uint16))
+        assert np.array_equal(dev2["v_cache"].cpu().numpy().view(np.uint16),
+                              dev["v_cache"].cpu().numpy().view(np.uint16))
 
 
 def _amax_scale(*arrays):
