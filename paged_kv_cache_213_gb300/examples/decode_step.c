@@ -7,7 +7,9 @@
  * in a shuffled pool), then on one stream:
  *   paged_decode_plan            how much workspace the automatic split needs;
  *   paged_decode_workspace_clear zero the new workspace's arrival counters;
- *   paged_decode_step            append each sequence's newest K/V, attend;
+ *   paged_decode_step_ex         append each sequence's newest K/V and attend,
+ *                                in one kernel (PKV_APPEND_NEWEST: token b is
+ *                                sequence b's newest token);
  *   paged_kv_get_error           read the device error word.
  * Inputs and results go to the file named by argv[1], so that a checker can
  * recompute the step independently (layout at write_all below).
@@ -152,9 +154,9 @@ int main(int argc, char **argv) {
     if (ws_bytes > 0) CUDA_OK(cudaMalloc(&d_ws, ws_bytes));
     PKV_OK_OR_DIE(paged_decode_workspace_clear(d_ws, ws_bytes, stream));
     const float scale = 1.0f / sqrtf((float)D);
-    PKV_OK_OR_DIE(paged_decode_step(d_kn, d_vn, d_sm, B, d_out, d_q, d_kc, d_vc, d_bt, d_cl, B,
-                                    MB, num_blocks, scale, H, HK, D, BS, MAX_LEN, 0, d_ws,
-                                    ws_bytes, d_lse, d_err, stream));
+    PKV_OK_OR_DIE(paged_decode_step_ex(d_kn, d_vn, d_sm, B, d_out, d_q, d_kc, d_vc, d_bt, d_cl,
+                                       B, MB, num_blocks, scale, H, HK, D, BS, MAX_LEN, 0, d_ws,
+                                       ws_bytes, d_lse, d_err, stream, PKV_APPEND_NEWEST));
     int32_t bits = -1;
     const int status = paged_kv_get_error(d_err, stream, &bits);
     if (status != PKV_OK && status != PKV_ERR_INDEX) PKV_OK_OR_DIE(status);
