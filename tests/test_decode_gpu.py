@@ -476,3 +476,23 @@ def test_fused_append_padding_and_broken_promises():
     got = _run_step(batch, pkv.PKV_APPEND_NEWEST, context_lens=cl)
     assert got[4] == pkv.PKV_ERRBIT_APPEND
     assert np.all(got[0][3] == 0) and np.all(np.isneginf(got[1][3]))
+
+
+def test_tables_ready_reads_q_after_the_wait():
+    """Under PKV_TABLES_READY the kernel before may write q: here q is the
+    output of the attention call just before (which lets its dependent launch
+    early), and the flagged call must read it only after that call is done."""
+    batch = wl.workload(2, poison=True)
+    dev = to_dev(batch)
+    pkv.paged_kv_append(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                        dev["v_cache"])
+    args = (dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+            batch.scale, batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.block_size)
+    mcl = batch.max_context_len
+    results = []
+    for flags in (0, pkv.PKV_TABLES_READY, pkv.PKV_TABLES_READY):
+        first = pkv.paged_decode_attention(dev["q"], *args, max_context_len=mcl)
+        second = pkv.paged_decode_attention(first, *args, max_context_len=mcl, flags=flags)
+        results.append(second.cpu().numpy())
+    for r in results[1:]:
+        assert np.array_equal(r.view(np.uint16), results[0].view(np.uint16))
