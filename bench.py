@@ -413,9 +413,9 @@ class Path:
                                        flags=self.attn_flags)
 
     def fused_step(self):
-        """The step is one paged_decode_step call (fp16, one query token, an
+        """The step is one paged_decode_step(_fp8) call (one query token, an
         append, no prefix groups), which takes step flags."""
-        return self.has_append and not self.fp8 and self.groups is None
+        return self.has_append and self.groups is None
 
     def set_step_flags(self, flags):
         """Flags of the one-call step; the launch count follows the library's
@@ -424,8 +424,11 @@ class Path:
             return
         self.step_flags = flags
         B, H, Hk, D, bs, MB, mcl = self._sizes
-        self.step_launches = self.pkv.step_launches(B, H, Hk, D, bs, MB, mcl, self.P,
-                                                    num_tokens=B, flags=flags)
+        if self.fp8:  # the E4M3 step: the append kernel, then the attention
+            self.step_launches = 2
+        else:
+            self.step_launches = self.pkv.step_launches(B, H, Hk, D, bs, MB, mcl, self.P,
+                                                        num_tokens=B, flags=flags)
 
     def flaggable(self):
         """The attention call takes launch flags (every entry point here has
@@ -440,6 +443,14 @@ class Path:
         pkv, bt, c = self.pkv, self.batch, self.copies[i]
         if not self.has_append:
             self.attend(i)
+            return
+        if self.fp8 and self.groups is None:
+            pkv.paged_decode_step_fp8(c["kn"], c["vn"], c["sm"], c["q"], c["kc"], c["vc"],
+                                      c["bt"], c["cl"], bt.scale, self.k_scale, self.v_scale,
+                                      bt.n_q_heads, bt.n_kv_heads, bt.head_dim, bt.block_size,
+                                      max_context_len=bt.max_context_len, out=c["out"],
+                                      workspace=c["work"], err_word=c["err"],
+                                      flags=self.step_flags)
             return
         if self.fp8:
             pkv.paged_kv_append_fp8(c["kn"], c["vn"], c["sm"], c["kc"], c["vc"], self.k_scale,
@@ -661,7 +672,39 @@ def per_config_rows(pkv, wl, torch, device, timer, peak, steps, rows_spec=PER_CO
             rows[key]["frac_plain_call"] = round(nbytes / (mp * 1e-3) / 1e9 / peak, 4)
         del path
         torch.cuda.empty_cache()
+    rows.update(fp8_step_row(pkv, wl, torch, device, timer, peak, steps))
     return rows
+
+
+def fp8_step_row(pkv, wl, torch, device, timer, peak, steps):
+    """The decode step over E4M3 caches on the LLaMA-3-8B-shaped layer:
+    paged_decode_step_fp8 (the quantizing append kernel, then the attention
+    with its prologue under the append), timed like the headline step."""
+    batch = wl.workload(2, poison=False)
+    nbytes = workload_bytes(batch, 1)["step"]
+    path = Path(pkv, wl, torch, batch, device, fp8=True)
+    path.set_step_flags(0)
+    for i in range(3):
+        timer.flush()
+        path.step(i % ROTATE)
+    torch.cuda.synchronize()
+    b2b = timer.back_to_back(lambda i: path.step(i % ROTATE), steps)
+    iso = timer.isolated(lambda i: path.step(i % ROTATE), min(steps, 200))
+    if any(path.errors()):
+        raise SystemExit("bench.py: device error word on the E4M3 step row")
+    ms, mi = statistics.fmean(b2b), statistics.fmean(iso)
+    row = {
+        "workload": wl.WORKLOADS[2], "entry": "paged_decode_step_fp8: append_f8_kernel, then "
+        "decode_balanced_kernel on E4M3 tiles",
+        "kv_dtype": "e4m3", "step_bytes": nbytes, "step_ms": round(ms, 5),
+        "step_gbs": round(nbytes / (ms * 1e-3) / 1e9, 2),
+        "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
+        "step_ms_isolated": round(mi, 5), "launches_per_step": path.step_launches,
+        "percentiles_ms": pcts(b2b),
+    }
+    del path
+    torch.cuda.empty_cache()
+    return {"w2_fp8_step": row}
 
 
 def run_ours(args):

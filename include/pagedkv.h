@@ -280,6 +280,7 @@ int paged_decode_step_ex(const void *k_new, const void *v_new, const int64_t *sl
 
 /*
  * How many kernels paged_decode_step_ex launches for these sizes and flags
+ * (fp16 caches; the E4M3 step launches the append and the attention)
  * (host only; the automatic split queries the current device, as
  * paged_decode_plan does): the append unless the attention does it
  * (PKV_APPEND_NEWEST on per-warp ranges), then one attention kernel, or two
@@ -569,6 +570,35 @@ int paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache
  * a NULL workspace with bytes, PKV_ERR_CUDA when the memset fails.
  */
 int paged_decode_workspace_clear(void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * One decode step over E4M3 caches: paged_kv_append_fp8 of num_tokens new
+ * tokens, then paged_decode_attention_fp8, on cuda_stream, with the same
+ * arguments, results and errors as those two calls (the attention's
+ * arguments are checked first, so a rejected call writes nothing).  The
+ * attention's prologue runs while the append drains.  paged_decode_step_fp8_ex
+ * accepts the flags of paged_decode_step_ex; the step keeps its two kernels
+ * under PKV_APPEND_NEWEST (folded into the E4M3 attention, which is bound by
+ * instruction issue, the append slowed it).  Other flag bits are rejected
+ * with PKV_ERR_INVALID_ARG.
+ */
+int paged_decode_step_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                          int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                          int max_blocks_per_seq, int64_t num_blocks, float scale,
+                          float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
+                          int head_dim, int block_size, int max_context_len, void *workspace,
+                          size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                          void *cuda_stream);
+int paged_decode_step_fp8_ex(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int num_tokens, void *out, const void *q, void *k_cache,
+                             void *v_cache, const int32_t *block_tables,
+                             const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                             int64_t num_blocks, float scale, float k_scale, float v_scale,
+                             int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                             int max_context_len, void *workspace, size_t workspace_bytes,
+                             float *lse_out, int32_t *err_word, void *cuda_stream,
+                             uint32_t flags);
 
 /*
  * Reads the device error word: waits for cuda_stream, copies *err_word to the

@@ -32,6 +32,7 @@ from .binding import (  # noqa: F401
     paged_kv_append,
     paged_kv_append_fp8,
     paged_decode_step,
+    paged_decode_step_fp8,
     paged_decode_workspace_clear,
     prefix_shared_plan,
     prefix_shared_plan_fp8,

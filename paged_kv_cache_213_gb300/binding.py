@@ -519,6 +519,60 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, 
     return out
 
 
+def paged_decode_step_fp8(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                          context_lens, scale, k_scale, v_scale, n_q_heads, n_kv_heads,
+                          head_dim, block_size, max_context_len=None, out=None, workspace=None,
+                          lse=None, err_word=None, flags=0):
+    """One decode step over E4M3 caches: paged_kv_append_fp8 then
+    paged_decode_attention_fp8 in one call.  flags (paged_decode_step_fp8_ex):
+    PKV_APPEND_NEWEST (token b is sequence b's newest: the attention kernel
+    quantizes and appends it, one launch) and PKV_TABLES_READY.  Returns out."""
+    lib = library()
+    fn = lib.paged_decode_step_fp8_ex
+    c = ctypes
+    p = c.c_void_p
+    fn.argtypes = [p, p, p, c.c_int, p, p, p, p, p, p, c.c_int, c.c_int, c.c_int64, c.c_float,
+                   c.c_float, c.c_float, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, p,
+                   c.c_size_t, p, p, p, c.c_uint32]
+    fn.restype = c.c_int
+    dev = q.device
+    for t, name, dt in ((k_new, "k_new", torch.float16), (v_new, "v_new", torch.float16),
+                        (slot_mapping, "slot_mapping", torch.int64), (q, "q", torch.float16),
+                        (k_cache, "k_cache", torch.uint8), (v_cache, "v_cache", torch.uint8),
+                        (block_tables, "block_tables", torch.int32),
+                        (context_lens, "context_lens", torch.int32)):
+        _need(t, name, dt, dev)
+    B, MB = block_tables.shape
+    T = k_new.shape[0]
+    if slot_mapping.shape != (T,) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new [T, Hk, d], slot_mapping [T]")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or \
+            k_cache.shape[1:] != (n_kv_heads, block_size, head_dim):
+        raise ValueError("caches must be [num_blocks, n_kv_heads, block_size, head_dim]")
+    mcl = 0 if max_context_len is None else int(max_context_len)
+    ws = decode_plan_fp8(B, n_q_heads, n_kv_heads, head_dim, block_size, MB, mcl)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, dev)
+    if workspace is None:
+        # zero-filled: the balanced split keeps arrival counters in it
+        workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(out), _ptr(q),
+                _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, MB,
+                k_cache.shape[0], float(scale), float(k_scale), float(v_scale), n_q_heads,
+                n_kv_heads, head_dim, block_size, mcl, _ptr(workspace), workspace.numel(),
+                _ptr(lse), _ptr(err_word), _stream_handle(dev), int(flags))
+    _check("paged_decode_step_fp8_ex", rc)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # multi-token (causal) attention: speculative verify, chunked prefill
 # ---------------------------------------------------------------------------

@@ -426,27 +426,16 @@ int make_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int paged_decode_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
-                          int block_size, int max_blocks_per_seq, int max_context_len,
-                          size_t *workspace_bytes_out) {
-    Plan plan{};
-    const int rc = make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
-                                 max_blocks_per_seq, max_context_len, &plan);
-    if (rc == PKV_OK && workspace_bytes_out) *workspace_bytes_out = plan.ws_bytes;
-    return rc;
-}
-
-int paged_decode_attention_fp8_ex(void *out, const void *q, const void *k_cache,
-                                  const void *v_cache, const int32_t *block_tables,
-                                  const int32_t *context_lens, int num_seqs,
-                                  int max_blocks_per_seq, int64_t num_blocks, float scale,
-                                  float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
-                                  int head_dim, int block_size, int max_context_len,
-                                  void *workspace, size_t workspace_bytes, float *lse_out,
-                                  int32_t *err_word, void *cuda_stream, uint32_t flags) {
-    if (flags & ~PKV_TABLES_READY) return PKV_ERR_INVALID_ARG;
+// paged_decode_attention_fp8; defer as decode_attention_impl.
+int fp8_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                       int max_blocks_per_seq, int64_t num_blocks, float scale, float k_scale,
+                       float v_scale, int n_q_heads, int n_kv_heads, int head_dim,
+                       int block_size, int max_context_len, void *workspace,
+                       size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                       void *cuda_stream, int defer) {
     if (num_blocks <= 0 || !std::isfinite(scale) || !std::isfinite(k_scale) ||
         !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
         return PKV_ERR_INVALID_ARG;
@@ -489,12 +478,93 @@ int paged_decode_attention_fp8_ex(void *out, const void *q, const void *k_cache,
     a.max_parts = 1;
     a.kv_fp8 = 1;
     a.v_scale = v_scale;
-    a.defer_dep_wait = (flags & PKV_TABLES_READY) ? 2 : 0;
+    a.defer_dep_wait = defer;
     a.first_wait_polls = pkv::test_wait_polls();
     const cudaError_t e =
         pkv::launch_decode_balanced(a, plan.bal, static_cast<cudaStream_t>(cuda_stream));
     if (e == cudaErrorInvalidValue) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_decode_plan_fp8(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                          int block_size, int max_blocks_per_seq, int max_context_len,
+                          size_t *workspace_bytes_out) {
+    Plan plan{};
+    const int rc = make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                                 max_blocks_per_seq, max_context_len, &plan);
+    if (rc == PKV_OK && workspace_bytes_out) *workspace_bytes_out = plan.ws_bytes;
+    return rc;
+}
+
+int paged_decode_attention_fp8_ex(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                  float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
+                                  int head_dim, int block_size, int max_context_len,
+                                  void *workspace, size_t workspace_bytes, float *lse_out,
+                                  int32_t *err_word, void *cuda_stream, uint32_t flags) {
+    if (flags & ~PKV_TABLES_READY) return PKV_ERR_INVALID_ARG;
+    return fp8_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              max_blocks_per_seq, num_blocks, scale, k_scale, v_scale, n_q_heads,
+                              n_kv_heads, head_dim, block_size, max_context_len, workspace,
+                              workspace_bytes, lse_out, err_word, cuda_stream,
+                              (flags & PKV_TABLES_READY) ? 2 : 0);
+}
+
+int paged_decode_step_fp8_ex(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int num_tokens, void *out, const void *q, void *k_cache,
+                             void *v_cache, const int32_t *block_tables,
+                             const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                             int64_t num_blocks, float scale, float k_scale, float v_scale,
+                             int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                             int max_context_len, void *workspace, size_t workspace_bytes,
+                             float *lse_out, int32_t *err_word, void *cuda_stream,
+                             uint32_t flags) {
+    if (flags & ~(PKV_TABLES_READY | PKV_APPEND_NEWEST)) return PKV_ERR_INVALID_ARG;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    // check the attention's arguments first so that a rejected call changes nothing
+    if (num_blocks <= 0 || !std::isfinite(scale) || !std::isfinite(k_scale) ||
+        !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    Plan plan{};
+    int rc = make_plan_fp8(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, max_context_len, &plan);
+    if (rc != PKV_OK) return rc;
+    if (num_seqs > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)))
+        return PKV_ERR_WORKSPACE;
+    // The append kernel, then the attention with its prologue under it.  The
+    // E4M3 attention is bound by instruction issue: an append folded into it
+    // (as the fp16 step does under PKV_APPEND_NEWEST) slowed every E4M3 call,
+    // so the flag is accepted and the step keeps its two kernels.
+    rc = paged_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens,
+                             n_kv_heads, head_dim, block_size, num_blocks, k_scale, v_scale,
+                             err_word, cuda_stream);
+    if (rc != PKV_OK) return rc;
+    return fp8_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              max_blocks_per_seq, num_blocks, scale, k_scale, v_scale, n_q_heads,
+                              n_kv_heads, head_dim, block_size, max_context_len, workspace,
+                              workspace_bytes, lse_out, err_word, cuda_stream,
+                              num_tokens > 0 ? 2 : 0);
+}
+
+int paged_decode_step_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                          int num_tokens, void *out, const void *q, void *k_cache, void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                          int max_blocks_per_seq, int64_t num_blocks, float scale,
+                          float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
+                          int head_dim, int block_size, int max_context_len, void *workspace,
+                          size_t workspace_bytes, float *lse_out, int32_t *err_word,
+                          void *cuda_stream) {
+    return paged_decode_step_fp8_ex(k_new, v_new, slot_mapping, num_tokens, out, q, k_cache,
+                                    v_cache, block_tables, context_lens, num_seqs,
+                                    max_blocks_per_seq, num_blocks, scale, k_scale, v_scale,
+                                    n_q_heads, n_kv_heads, head_dim, block_size, max_context_len,
+                                    workspace, workspace_bytes, lse_out, err_word, cuda_stream, 0);
 }
 
 int paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,

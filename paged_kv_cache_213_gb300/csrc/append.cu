@@ -11,6 +11,7 @@
 
 #include "pagedkv.h"
 #include "pkv_internal.h"
+#include "e4m3_quant.cuh"
 #include "pkv_ptx.cuh"
 
 namespace pkv {
@@ -107,33 +108,12 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
 }  // namespace pkv
 
 // FP8 KV cache append (the quantized KV cache the "Roadmap: vLLM-style
-// serving features for TornadoVM batched decode" page lists as future work;
-// E4M3 with one scale per cache tensor is this library's reading): each
-// value is stored as E4M3(x / scale), the quotient one correctly rounded
-// fp32 division, the conversion round-to-nearest-even with finite overflow
-// saturated to +-448 (the hardware cvt.rn.satfinite).  One thread turns 16
-// fp16 values of K and of V (two 16-byte loads each) into one 16-byte store.
+// serving features for TornadoVM batched decode" page lists as future work):
+// each value is stored as E4M3(x / scale) by quantize16 (e4m3_quant.cuh).
+// One thread turns 16 fp16 values of K and of V (two 16-byte loads each) into
+// one 16-byte store.
 namespace pkv {
 namespace {
-
-__device__ __forceinline__ uint4 quantize16(const uint4 &lo, const uint4 &hi, float scale) {
-    const __half2 *h0 = reinterpret_cast<const __half2 *>(&lo);
-    const __half2 *h1 = reinterpret_cast<const __half2 *>(&hi);
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half2 a = i < 2 ? h0[2 * i] : h1[2 * i - 4];
-        const __half2 b = i < 2 ? h0[2 * i + 1] : h1[2 * i - 3];
-        const float2 fa = __half22float2(a);
-        const float2 fb = __half22float2(b);
-        const __nv_fp8x2_storage_t ca = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(fa.x, scale), __fdiv_rn(fa.y, scale)), __NV_SATFINITE, __NV_E4M3);
-        const __nv_fp8x2_storage_t cb = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(fb.x, scale), __fdiv_rn(fb.y, scale)), __NV_SATFINITE, __NV_E4M3);
-        w[i] = static_cast<uint32_t>(ca) | (static_cast<uint32_t>(cb) << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
 
 __global__ void __launch_bounds__(256)
     append_f8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,

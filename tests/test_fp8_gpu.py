@@ -284,3 +284,69 @@ def test_fp8_tables_ready_flag(cfg):
         assert np.array_equal(o.view(np.uint16), outs[0].view(np.uint16))
     ref = oracle_f8(batch, kc8, vc8, ks, vs)
     assert_close(outs[0], ref["out"], what=f"flagged fp8 workload {cfg}")
+
+
+def _step8(batch, kc8, vc8, ks, vs, flags, slot_mapping=None, context_lens=None):
+    """paged_decode_step_fp8 on fresh device copies: out, lse, caches, bits."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lse = torch.full((batch.num_seqs, batch.n_q_heads), float("nan"), device="cuda")
+    kc, vc = _t(kc8), _t(vc8)
+    sm = _t(batch.slot_mapping if slot_mapping is None else slot_mapping)
+    cl = _t(batch.context_lens if context_lens is None else context_lens)
+    out = pkv.paged_decode_step_fp8(
+        _t(batch.k_new), _t(batch.v_new), sm, _t(batch.q), kc, vc, _t(batch.block_tables), cl,
+        batch.scale, ks, vs, batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
+        batch.block_size, max_context_len=batch.max_context_len, lse=lse, err_word=err,
+        flags=flags)
+    bits = pkv.get_error(err)
+    return out.cpu().numpy(), lse.cpu().numpy(), kc.cpu().numpy(), vc.cpu().numpy(), bits
+
+
+STEP_FLAGS = (pkv.PKV_APPEND_NEWEST, pkv.PKV_APPEND_NEWEST | pkv.PKV_TABLES_READY)
+
+
+def _same8(a, b):
+    return np.array_equal(np.ascontiguousarray(a).view(np.uint8),
+                          np.ascontiguousarray(b).view(np.uint8))
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_fp8_step_matches_separate_calls(cfg):
+    """paged_decode_step_fp8 (the append kernel, then the attention with its
+    prologue under the append): codes, output and lse bit-identical to the
+    separate calls, with and without the step flags."""
+    batch = wl.workload(cfg, poison=True)
+    ks, vs = _scales(batch)
+    kc8, vc8 = _caches8(batch, ks, vs)
+    two = _step8(batch, kc8, vc8, ks, vs, 0)
+    assert two[4] == 0
+    sep = gpu_f8(batch, kc8, vc8, ks, vs)
+    assert _same8(two[0], sep["out"]) and _same8(two[2], sep["k_cache"])
+    assert _same8(two[3], sep["v_cache"])
+    for flags in STEP_FLAGS:
+        got = _step8(batch, kc8, vc8, ks, vs, flags)
+        assert got[4] == 0, flags
+        for x, y in zip(got[:4], two[:4]):
+            assert _same8(x, y), flags
+    ref = oracle_f8(batch, kc8, vc8, ks, vs)
+    assert_close(two[0], ref["out"], what=f"fp8 step workload {cfg}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_fp8_step_edge_shapes(d, g, bs):
+    rng = np.random.default_rng(700 + d + 10 * g + bs)
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 64, 130, 300, 1000]
+    batch = wl.make_batch("f8step", lens, 2 * g, 2, d, bs, rng, append=True, poison=True)
+    ks, vs = _scales(batch)
+    kc8, vc8 = _caches8(batch, ks, vs)
+    two = _step8(batch, kc8, vc8, ks, vs, 0)
+    assert two[4] == 0
+    for flags in STEP_FLAGS:
+        got = _step8(batch, kc8, vc8, ks, vs, flags)
+        assert got[4] == 0
+        for x, y in zip(got[:4], two[:4]):
+            assert _same8(x, y), (d, g, bs, flags)
+    assert_close(two[0], oracle_f8(batch, kc8, vc8, ks, vs)["out"],
+                 what=f"fp8 step d={d} g={g} bs={bs}")

@@ -153,6 +153,17 @@ def test_e4m3_random(seed):
     what = f"seed {seed}: d={d} g={g} Hk={hk} bs={bs} B={B}"
     assert pkv.get_error(err) == 0, what
     assert np.array_equal(kc.cpu().numpy(), rk) and np.array_equal(vc.cpu().numpy(), rv), what
+    if append:  # the one-call step: the same codes and output as append + attention
+        kc2, vc2 = _t(kc8), _t(vc8)
+        stepped = pkv.paged_decode_step_fp8(
+            _t(batch.k_new), _t(batch.v_new), _t(batch.slot_mapping), _t(batch.q), kc2, vc2,
+            _t(batch.block_tables), _t(batch.context_lens), batch.scale, ks, vs, g * hk, hk, d,
+            bs, max_context_len=batch.max_context_len, err_word=err,
+            flags=pkv.PKV_APPEND_NEWEST | pkv.PKV_TABLES_READY)
+        assert pkv.get_error(err) == 0, what
+        assert np.array_equal(kc2.cpu().numpy(), rk) and np.array_equal(vc2.cpu().numpy(), rv)
+        assert np.array_equal(stepped.cpu().numpy().view(np.uint16),
+                              out.cpu().numpy().view(np.uint16)), what
     assert_close(out.cpu().numpy(), ref, what=what)
     got_lse = lse.cpu().numpy().astype(np.float64)
     finite = np.isfinite(ref_lse)
