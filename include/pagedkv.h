@@ -164,7 +164,10 @@ int paged_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
  * (flash-decoding split).
  * L_b = 0 gives out = 0 and lse = -inf.
  *
- *  out            device fp16 [num_seqs][n_q_heads][head_dim]
+ *  out            fp16 [num_seqs][n_q_heads][head_dim], device memory or pinned
+ *                 (page-locked, mapped) host memory: the kernels write it with
+ *                 plain stores, so with a host buffer the results reach the
+ *                 host as they are written, with no copy after the call
  *  q              device fp16 [num_seqs][n_q_heads][head_dim]
  *  k_cache, v_cache, block_tables, context_lens   as in the layout notes
  *  scale          multiplies q . K before the softmax (1/sqrt(head_dim) usually)

@@ -117,6 +117,18 @@ def _need(t: torch.Tensor, name: str, dtype, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _need_out(out, dev):
+    """out: fp16 on the call's device, or a pinned host tensor, which the
+    kernels write directly (plain stores into mapped host memory)."""
+    if isinstance(out, torch.Tensor) and not out.is_cuda and out.is_pinned():
+        if out.dtype != torch.float16:
+            raise TypeError(f"out must be {torch.float16}, got {out.dtype}")
+        if not out.is_contiguous():
+            raise ValueError("out must be contiguous")
+        return
+    _need(out, "out", torch.float16, dev)
+
+
 def paged_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, err_word=None):
     """Write k_new/v_new [T, Hk, d] (fp16) into slots slot_mapping [T] (int64)
     of k_cache/v_cache [NB, Hk, bs, d] (fp16), in place, on the current stream."""
@@ -194,7 +206,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     if out is None:
         out = torch.empty_like(q)
     else:
-        _need(out, "out", torch.float16, dev)
+        _need_out(out, dev)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     if lse is not None:
@@ -699,7 +711,7 @@ def paged_decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tab
     if out is None:
         out = torch.empty_like(q)
     else:
-        _need(out, "out", torch.float16, dev)
+        _need_out(out, dev)
     if ws > 0:
         if workspace is None:
             # zero-filled: the balanced split keeps arrival counters in it

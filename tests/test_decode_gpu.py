@@ -496,3 +496,36 @@ def test_tables_ready_reads_q_after_the_wait():
         results.append(second.cpu().numpy())
     for r in results[1:]:
         assert np.array_equal(r.view(np.uint16), results[0].view(np.uint16))
+
+
+def test_pinned_host_out():
+    """out may be pinned host memory: the kernels store the results into it
+    directly.  The step (one launch and two kernels) and the attention call
+    give the same bits as with device memory."""
+    batch = wl.workload(2, poison=True)
+    shape = (batch.num_seqs, batch.n_q_heads, batch.head_dim)
+    outs = []
+    for where in ("device", "host"):
+        for flags in (0, pkv.PKV_APPEND_NEWEST):
+            dev = to_dev(batch)
+            out = torch.empty(shape, dtype=torch.float16, pin_memory=True) if where == "host" \
+                else None
+            got = pkv.paged_decode_step(dev["k_new"], dev["v_new"], dev["slot_mapping"],
+                                        dev["q"], dev["k_cache"], dev["v_cache"],
+                                        dev["block_tables"], dev["context_lens"], batch.scale,
+                                        batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
+                                        batch.block_size, max_context_len=batch.max_context_len,
+                                        out=out, flags=flags)
+            att_out = torch.empty(shape, dtype=torch.float16, pin_memory=True) \
+                if where == "host" else None
+            att = pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                             dev["block_tables"], dev["context_lens"],
+                                             batch.scale, batch.n_q_heads, batch.n_kv_heads,
+                                             batch.head_dim, batch.block_size,
+                                             max_context_len=batch.max_context_len, out=att_out)
+            torch.cuda.synchronize()
+            outs.append((got.cpu().numpy().copy(), att.cpu().numpy().copy()))
+    for step_out, att_out in outs[1:]:
+        assert np.array_equal(step_out.view(np.uint16), outs[0][0].view(np.uint16))
+        assert np.array_equal(att_out.view(np.uint16), outs[0][1].view(np.uint16))
+    assert_close(outs[0][0], oracle_step(batch)["out"], what="pinned host out")
