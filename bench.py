@@ -840,9 +840,12 @@ def run_ours(args):
         # buffer (plain stores over the host link); other steps copy it after.
         zero_copy_out = path.fused_step() and not fp8
 
-        def e2e_body(i):
+        def e2e_body(i, engine=False):
             stage_dev, stage_host, out_host = stages[i % ROTATE]
-            stage_dev.copy_(stage_host, non_blocking=True)
+            if engine:  # the copy engine (cudaMemcpyAsync), for comparison
+                stage_dev.copy_(stage_host, non_blocking=True)
+            else:  # the library's copy kernel: one 16-byte piece per thread
+                pkv.paged_copy_in(stage_dev, stage_host)
             if zero_copy_out:
                 path.step(i % ROTATE, out=out_host)
             else:
@@ -850,6 +853,7 @@ def run_ours(args):
                 out_host.copy_(path.copies[i % ROTATE]["out"], non_blocking=True)
         e2e_ms_list = timer.back_to_back(e2e_body, args.steps)
         e2e_iso_list = timer.isolated(e2e_body, args.steps)
+        e2e_engine_list = timer.back_to_back(lambda i: e2e_body(i, True), args.steps)
         # the host buffers hold what a device-memory step computes, bit for bit
         torch.cuda.synchronize()
         for k in range(ROTATE):
@@ -866,10 +870,13 @@ def run_ours(args):
         e2e = {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
                "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(e2e_ms, 5),
                "value_isolated": round(e2e_iso_val, 2),
+               "ms_per_step_copy_engine": round(statistics.fmean(e2e_engine_list), 5),
                "ms_per_step_isolated": round(e2e_iso_ms, 5),
-               "timing": "every step: pinned-host -> device copy of the step's inputs, the step "
-                         "(paged_decode_step with the step flags), whose kernel writes out "
-                         "into pinned host memory (no copy after it); steps back to "
+               "timing": "every step: pinned-host -> device copy of the step's inputs by the "
+                         "library's copy kernel (paged_copy_in; ms_per_step_copy_engine: the "
+                         "same steps with cudaMemcpyAsync instead), the step (paged_decode_step "
+                         "with the step flags), whose kernel writes out into pinned host memory "
+                         "(no copy after it); steps back to "
                          "back over the four input copies (value), or each its own timed region "
                          "after an L2 flush (value_isolated)"}
 

@@ -564,6 +564,16 @@ int paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache
                                    int32_t *err_word, void *cuda_stream);
 
 /*
+ * Copies bytes from src to dst on cuda_stream with a kernel in which every
+ * thread moves one 16-byte piece.  src may be pinned (page-locked, mapped)
+ * host memory: a decode step's inputs staged on the host then cross the host
+ * link in about one round trip, and the copy is a kernel that the step's own
+ * launch follows on the stream.  Both pointers 16-byte aligned, bytes a
+ * multiple of 16 (PKV_ERR_INVALID_ARG otherwise); bytes = 0 is a no-op.
+ */
+int paged_copy_in(void *dst, const void *src, size_t bytes, void *cuda_stream);
+
+/*
  * Zeroes the arrival counters of a workspace on cuda_stream: the first
  * min(workspace_bytes, PKV_WORKSPACE_COUNTER_BYTES) bytes (one
  * cudaMemsetAsync; no allocation, no host wait, so it may be captured in a

@@ -34,6 +34,7 @@ from .binding import (  # noqa: F401
     paged_decode_step,
     paged_decode_step_fp8,
     paged_decode_workspace_clear,
+    paged_copy_in,
     prefix_shared_plan,
     prefix_shared_plan_fp8,
     status_string,

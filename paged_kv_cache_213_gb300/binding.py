@@ -277,6 +277,23 @@ def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_le
     return out
 
 
+def paged_copy_in(dst: torch.Tensor, src: torch.Tensor):
+    """dst (device) <- src (device or pinned host) by a library kernel, on the
+    current stream: both contiguous uint8 of the same size, a multiple of 16."""
+    _need(dst, "dst", torch.uint8)
+    if not (isinstance(src, torch.Tensor) and (src.is_cuda or src.is_pinned())):
+        raise ValueError("src must be a CUDA tensor or pinned host memory")
+    if src.dtype != torch.uint8 or not src.is_contiguous() or src.numel() != dst.numel():
+        raise ValueError("src must be contiguous uint8 of dst's size")
+    lib = library()
+    fn = lib.paged_copy_in
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    with torch.cuda.device(dst.device):
+        _check("paged_copy_in", fn(_ptr(dst), _ptr(src), dst.numel(),
+                                   _stream_handle(dst.device)))
+
+
 def paged_decode_workspace_clear(workspace: torch.Tensor):
     """Zero a workspace's arrival counters on the current stream (needed after a
     call flagged PKV_ERRBIT_TIMEOUT or PKV_ERRBIT_WORKSPACE)."""

@@ -1073,6 +1073,16 @@ int paged_kv_get_error(const int32_t *err_word, void *cuda_stream, int32_t *bits
     return host == 0 ? PKV_OK : PKV_ERR_INDEX;
 }
 
+int paged_copy_in(void *dst, const void *src, size_t bytes, void *cuda_stream) {
+    if (bytes == 0) return PKV_OK;
+    if (!dst || !src || !aligned(dst, 16) || !aligned(src, 16) || bytes % 16 != 0)
+        return PKV_ERR_INVALID_ARG;
+    return pkv::launch_copy_in(dst, src, bytes, static_cast<cudaStream_t>(cuda_stream)) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 int paged_kv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst,
                          const int32_t *tokens, int num_copies, int n_kv_heads, int head_dim,
                          int block_size, int64_t num_blocks, int32_t *err_word,

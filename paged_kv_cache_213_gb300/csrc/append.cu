@@ -44,6 +44,24 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
+// One 16-byte piece per thread, every piece in flight at once: from mapped
+// host memory the copy costs about one round trip over the host link.
+__global__ void __launch_bounds__(256)
+    copy_in_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, long long n) {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_copy_in(void *dst, const void *src, size_t bytes, cudaStream_t stream) {
+    const long long n = static_cast<long long>(bytes / 16);
+    if (n == 0) return cudaSuccess;
+    const long long blocks = (n + 255) / 256;
+    copy_in_kernel<<<static_cast<unsigned>(blocks < 65535 ? blocks : 65535), 256, 0, stream>>>(
+        static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream) {
     const int chunks = a.head_dim / 8;
     const long long total = static_cast<long long>(a.num_tokens) * a.n_kv_heads * chunks;

@@ -159,6 +159,9 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts);
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
+// dst <- src, 16 bytes per thread (both 16-byte aligned, bytes a multiple of
+// 16); src may be mapped host memory.
+cudaError_t launch_copy_in(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 // FP8 (E4M3) caches: k_cache / v_cache hold one byte per value, head_dim % 16 == 0.
 cudaError_t launch_append_f8(const AppendArgs &a, float k_scale, float v_scale,
                              cudaStream_t stream);

@@ -63,6 +63,18 @@ def test_python_constants_match_the_header():
     assert d["PKV_WORKSPACE_COUNTER_BYTES"] < d["PKV_NOALLOC_SCRATCH_BYTES"]
 
 
+def test_copy_in_host_checks(lib):
+    """Zero bytes is a no-op; NULL, misaligned or ragged copies are rejected,
+    all before any CUDA call."""
+    fn = lib.paged_copy_in
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    assert fn(None, None, 0, None) == 0
+    assert fn(None, ctypes.c_void_p(4096), 64, None) == -1
+    assert fn(ctypes.c_void_p(4096), ctypes.c_void_p(4104), 64, None) == -1  # misaligned
+    assert fn(ctypes.c_void_p(4096), ctypes.c_void_p(8192), 40, None) == -1  # not 16n bytes
+
+
 def test_workspace_clear_host_checks(lib):
     """Zero bytes is a no-op and a NULL workspace with bytes is rejected, both
     before any CUDA call."""

@@ -529,3 +529,19 @@ def test_pinned_host_out():
         assert np.array_equal(step_out.view(np.uint16), outs[0][0].view(np.uint16))
         assert np.array_equal(att_out.view(np.uint16), outs[0][1].view(np.uint16))
     assert_close(outs[0][0], oracle_step(batch)["out"], what="pinned host out")
+
+
+def test_copy_in_from_pinned_and_device_memory():
+    """paged_copy_in moves bytes into device memory with a kernel, from pinned
+    host memory or from device memory, bit for bit."""
+    rng = np.random.default_rng(5)
+    for n in (16, 4096, 409600, 1 << 22):
+        host = torch.from_numpy(rng.integers(0, 256, n, dtype=np.uint8)).pin_memory()
+        dst = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        pkv.paged_copy_in(dst, host)
+        torch.cuda.synchronize()
+        assert torch.equal(dst.cpu(), host)
+        dst2 = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        pkv.paged_copy_in(dst2, dst)
+        torch.cuda.synchronize()
+        assert torch.equal(dst2, dst)
